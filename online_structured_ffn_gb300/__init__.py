@@ -1,0 +1,296 @@
+"""Python binding of libpopffn.so: partition-guided online structured pruning (POP) of a gated-MLP FFN.
+
+This module only marshals arguments: every step of prefill, partition and decode
+runs in the library's sm_103a kernels. PyTorch supplies device memory
+(``tensor.data_ptr()``) and streams (``torch.cuda.current_stream().cuda_stream``).
+There is no CPU fallback: importing fails loudly when the library is missing.
+
+The names mirror the C ABI in ``include/pop_ffn.h`` (``pop_ffn_create``,
+``pop_prefill_partition``, ``pop_decode_step``, ``pop_ffn_dense_ref``, ...);
+``PopFFN`` wraps a handle for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpopffn.so")
+
+POP_OK, POP_ERR_INVALID_ARG, POP_ERR_STATE, POP_ERR_CUDA, POP_ERR_OOM, POP_ERR_TIMEOUT, POP_ERR_UNSUPPORTED, \
+    POP_ERR_DEVICE = range(8)
+POP_MAX_D, POP_MAX_D_FF, POP_MAX_BATCH = 16384, 49152, 64
+
+
+class pop_config(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("D_FF", ctypes.c_int), ("r", ctypes.c_double), ("gamma", ctypes.c_double),
+                ("period", ctypes.c_int), ("max_batch", ctypes.c_int), ("max_prefill_tokens", ctypes.c_int),
+                ("out_f32", ctypes.c_int)]
+
+
+class pop_counts(ctypes.Structure):
+    _fields_ = [("n_P", ctypes.c_int), ("n_R", ctypes.c_int), ("n_C", ctypes.c_int), ("keep", ctypes.c_int),
+                ("k", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class PopError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+_vp, _i32, _f64, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_uint64
+_ip, _fp = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float)
+SIGNATURES = {
+    "pop_region_counts": (_i32, [_i32, _f64, _f64, ctypes.POINTER(pop_counts)]),
+    "pop_ffn_create": (_i32, [ctypes.POINTER(pop_config), _vp, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "pop_ffn_destroy": (None, [_vp]),
+    "pop_ffn_counts": (_i32, [_vp, ctypes.POINTER(pop_counts)]),
+    "pop_prefill_partition": (_i32, [_vp, _vp, _i32, _vp, _vp]),
+    "pop_partition_from_importance": (_i32, [_vp, _vp, _vp]),
+    "pop_set_partition": (_i32, [_vp, _ip, _ip, _ip, _vp]),
+    "pop_decode_step": (_i32, [_vp, _vp, _i32, _vp, _vp]),
+    "pop_ffn_dense_ref": (_i32, [_vp, _vp, _i32, _vp, _vp]),
+    "pop_get_partition": (_i32, [_vp, _ip, _ip, _ip]),
+    "pop_get_importance": (_i32, [_vp, _fp, _fp]),
+    "pop_get_selected": (_i32, [_vp, _ip, _ip]),
+    "pop_get_scores": (_i32, [_vp, _fp, _fp]),
+    "pop_get_step": (_i32, [_vp, _ip]),
+    "pop_set_wait_limit": (_i32, [_vp, _u64]),
+    "pop_check": (_i32, [_vp]),
+    "pop_last_error": (ctypes.c_char_p, [_vp]),
+    "pop_status_string": (ctypes.c_char_p, [_i32]),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libpopffn.so and declares its signatures. Raises ImportError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_name(s: int) -> str:
+    names = ["POP_OK", "POP_ERR_INVALID_ARG", "POP_ERR_STATE", "POP_ERR_CUDA", "POP_ERR_OOM", "POP_ERR_TIMEOUT",
+             "POP_ERR_UNSUPPORTED", "POP_ERR_DEVICE"]
+    return names[s] if 0 <= s < len(names) else f"status {s}"
+
+
+def _check(status: int, handle=None):
+    if status != POP_OK:
+        msg = load_library().pop_last_error(handle)
+        raise PopError(status, msg.decode() if msg else "")
+
+
+def _ptr(t):
+    """Device address of a tensor (or an int already holding one, or None)."""
+    if t is None or isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _int_array(a):
+    import numpy as np
+    arr = np.ascontiguousarray(a, dtype=np.int32)
+    if arr.size == 0:
+        arr = np.zeros(1, dtype=np.int32)
+    return arr, arr.ctypes.data_as(_ip)
+
+
+# ------------------------------------------------------------------ C-ABI mirrors
+
+def pop_region_counts(N: int, r: float, gamma: float) -> pop_counts:
+    out = pop_counts()
+    _check(load_library().pop_region_counts(N, r, gamma, ctypes.byref(out)))
+    return out
+
+
+def pop_ffn_create(cfg: pop_config, Wg, W1, W2, stream=None) -> int:
+    h = ctypes.c_void_p()
+    _check(load_library().pop_ffn_create(ctypes.byref(cfg), _ptr(Wg), _ptr(W1), _ptr(W2), _stream(stream),
+                                         ctypes.byref(h)))
+    return h.value
+
+
+def pop_ffn_destroy(h) -> None:
+    load_library().pop_ffn_destroy(h)
+
+
+def pop_ffn_counts(h) -> pop_counts:
+    out = pop_counts()
+    _check(load_library().pop_ffn_counts(h, ctypes.byref(out)), h)
+    return out
+
+
+def pop_prefill_partition(h, X, M: int, Y=None, stream=None) -> None:
+    _check(load_library().pop_prefill_partition(h, _ptr(X), M, _ptr(Y), _stream(stream)), h)
+
+
+def pop_partition_from_importance(h, importance, stream=None) -> None:
+    _check(load_library().pop_partition_from_importance(h, _ptr(importance), _stream(stream)), h)
+
+
+def pop_set_partition(h, R, C, P, stream=None) -> None:
+    (_r, rp), (_c, cp), (_p, pp) = _int_array(R), _int_array(C), _int_array(P)
+    _check(load_library().pop_set_partition(h, rp, cp, pp, _stream(stream)), h)
+
+
+def pop_decode_step(h, x, B: int, y, stream=None) -> None:
+    _check(load_library().pop_decode_step(h, _ptr(x), B, _ptr(y), _stream(stream)), h)
+
+
+def pop_ffn_dense_ref(h, X, M: int, Y, stream=None) -> None:
+    _check(load_library().pop_ffn_dense_ref(h, _ptr(X), M, _ptr(Y), _stream(stream)), h)
+
+
+def pop_get_partition(h):
+    import numpy as np
+    c = pop_ffn_counts(h)
+    R, C, P = (np.zeros(max(n, 1), dtype=np.int32) for n in (c.n_R, c.n_C, c.n_P))
+    _check(load_library().pop_get_partition(h, R.ctypes.data_as(_ip), C.ctypes.data_as(_ip), P.ctypes.data_as(_ip)),
+           h)
+    return R[:c.n_R], C[:c.n_C], P[:c.n_P]
+
+
+def pop_get_importance(h):
+    import numpy as np
+    c = pop_ffn_counts(h)
+    N = c.n_P + c.n_R + c.n_C
+    I, ss = np.zeros(N, dtype=np.float32), np.zeros(N, dtype=np.float32)
+    _check(load_library().pop_get_importance(h, I.ctypes.data_as(_fp), ss.ctypes.data_as(_fp)), h)
+    return I, ss
+
+
+def pop_get_selected(h):
+    import numpy as np
+    c = pop_ffn_counts(h)
+    S = np.zeros(max(c.k, 1), dtype=np.int32)
+    k = ctypes.c_int()
+    _check(load_library().pop_get_selected(h, ctypes.byref(k), S.ctypes.data_as(_ip)), h)
+    return S[:k.value]
+
+
+def pop_get_scores(h):
+    import numpy as np
+    c = pop_ffn_counts(h)
+    a, m = np.zeros(max(c.n_C, 1), dtype=np.float32), np.zeros(max(c.n_C, 1), dtype=np.float32)
+    _check(load_library().pop_get_scores(h, a.ctypes.data_as(_fp), m.ctypes.data_as(_fp)), h)
+    return a[:c.n_C], m[:c.n_C]
+
+
+def pop_get_step(h) -> int:
+    s = ctypes.c_int()
+    _check(load_library().pop_get_step(h, ctypes.byref(s)), h)
+    return s.value
+
+
+def pop_set_wait_limit(h, ns: int) -> None:
+    _check(load_library().pop_set_wait_limit(h, ns), h)
+
+
+def pop_check(h) -> None:
+    _check(load_library().pop_check(h), h)
+
+
+# ------------------------------------------------------------------ convenience wrapper
+
+class PopFFN:
+    """One gated-MLP layer with POP pruning, backed by a pop_ffn handle.
+
+    Wg, W1: torch bf16 [D_FF, D] on the current CUDA device; W2: bf16 [D, D_FF].
+    """
+
+    def __init__(self, Wg, W1, W2, r: float, gamma: float = 0.1, period: int = 1, max_batch: int = 1,
+                 max_prefill_tokens: int = 2048, out_f32: bool = True, stream=None):
+        N, D = Wg.shape
+        self.handle = None
+        self.cfg = pop_config(D=D, D_FF=N, r=r, gamma=gamma, period=period, max_batch=max_batch,
+                              max_prefill_tokens=max_prefill_tokens, out_f32=1 if out_f32 else 0)
+        self.D, self.N = D, N
+        self.handle = pop_ffn_create(self.cfg, Wg, W1, W2, stream)
+        self.counts = pop_ffn_counts(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            pop_ffn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.cfg.out_f32 else torch.bfloat16
+
+    def prefill_partition(self, X, Y=None, stream=None):
+        pop_prefill_partition(self.handle, X, X.shape[0], Y, stream)
+
+    def partition_from_importance(self, importance, stream=None):
+        pop_partition_from_importance(self.handle, importance, stream)
+
+    def set_partition(self, R, C, P, stream=None):
+        pop_set_partition(self.handle, R, C, P, stream)
+
+    def decode_step(self, x, y=None, stream=None):
+        import torch
+        if y is None:
+            y = torch.empty((x.shape[0], self.D), dtype=self.out_dtype(), device=x.device)
+        pop_decode_step(self.handle, x, x.shape[0], y, stream)
+        return y
+
+    def dense_ref(self, X, Y=None, stream=None):
+        import torch
+        if Y is None:
+            Y = torch.empty((X.shape[0], self.D), dtype=self.out_dtype(), device=X.device)
+        pop_ffn_dense_ref(self.handle, X, X.shape[0], Y, stream)
+        return Y
+
+    def partition(self):
+        return pop_get_partition(self.handle)
+
+    def importance(self):
+        return pop_get_importance(self.handle)
+
+    def selected(self):
+        return pop_get_selected(self.handle)
+
+    def scores(self):
+        return pop_get_scores(self.handle)
+
+    def step_count(self):
+        return pop_get_step(self.handle)
+
+    def set_wait_limit(self, ns: int):
+        pop_set_wait_limit(self.handle, ns)
+
+    def check(self):
+        pop_check(self.handle)
+
+
+load_library()

@@ -1,0 +1,424 @@
+// C-ABI of the POP FFN library (declared in include/pop_ffn.h): handle, argument checks, device
+// scratch, and the launch sequences of prefill, decode and the dense path.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "pop_ffn.h"
+#include "pop_internal.h"
+
+using namespace pop;
+
+struct pop_ffn {
+  pop_config cfg{};
+  pop_counts cnt{};
+  int D = 0, N = 0;
+  int device = 0, num_sms = 0;
+  // packed weights and norms
+  uint16_t* Wp = nullptr;
+  float* n2 = nullptr;
+  // prefill scratch
+  uint16_t* Z = nullptr;
+  int ldZ = 0, Mcap = 0;
+  float* part = nullptr;
+  int ldPart = 0;
+  float* sumsq = nullptr;
+  float* I = nullptr;
+  PrefillMaps maps{};
+  // partition: rc = [C ascending | R ascending], P ascending; idx_all = 0..N-1
+  int* rc = nullptr;
+  int* P = nullptr;
+  int* idx_all = nullptr;
+  // decode scratch
+  float* z = nullptr;  // [max_batch][N]
+  float* scores = nullptr;
+  float* memory = nullptr;
+  int* S = nullptr;
+  float* ypart = nullptr;
+  int ypart_parts = 0;  // capacity in units of D floats
+  int* step = nullptr;
+  unsigned* err = nullptr;
+  bool partitioned = false;
+  bool selected = false;
+  uint64_t wait_ns = 2000000000ull;
+  std::string msg;
+};
+
+namespace {
+thread_local std::string g_msg;
+
+pop_status fail(pop_ffn* h, pop_status s, const std::string& m) {
+  (h ? h->msg : g_msg) = m;
+  return s;
+}
+
+pop_status cuda_fail(pop_ffn* h, cudaError_t e, const char* where) {
+  return fail(h, e == cudaErrorMemoryAllocation ? POP_ERR_OOM : POP_ERR_CUDA,
+              std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define POP_CUDA(h, call)                                  \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+long long round_half_even(double v) { return static_cast<long long>(std::nearbyint(v)); }
+
+template <class T>
+cudaError_t dalloc(T** p, size_t count) {
+  if (count == 0) count = 1;
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+PackedWeights packed(const pop_ffn* h) { return PackedWeights{h->Wp, h->n2, h->D, h->N}; }
+
+void free_all(pop_ffn* h) {
+  void* ptrs[] = {h->Wp, h->n2, h->Z, h->part, h->sumsq, h->I, h->rc, h->P, h->idx_all,
+                  h->z,  h->scores, h->memory, h->S, h->ypart, h->step, h->err};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+__global__ void k_iota(int* a, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) a[i] = i;
+}
+}  // namespace
+
+extern "C" {
+
+const char* pop_status_string(pop_status s) {
+  switch (s) {
+    case POP_OK: return "POP_OK";
+    case POP_ERR_INVALID_ARG: return "POP_ERR_INVALID_ARG";
+    case POP_ERR_STATE: return "POP_ERR_STATE";
+    case POP_ERR_CUDA: return "POP_ERR_CUDA";
+    case POP_ERR_OOM: return "POP_ERR_OOM";
+    case POP_ERR_TIMEOUT: return "POP_ERR_TIMEOUT";
+    case POP_ERR_UNSUPPORTED: return "POP_ERR_UNSUPPORTED";
+    case POP_ERR_DEVICE: return "POP_ERR_DEVICE";
+  }
+  return "POP_ERR_UNKNOWN";
+}
+
+const char* pop_last_error(pop_ffn_t h) { return h ? h->msg.c_str() : g_msg.c_str(); }
+
+pop_status pop_region_counts(int N, double r, double gamma, pop_counts* out) {
+  if (!out) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_region_counts: out is NULL");
+  if (!(r >= 0.0 && r <= 1.0) || !(gamma >= 0.0) || N < 0)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_region_counts: need 0 <= r <= 1, gamma >= 0, N >= 0");
+  double lo = r - gamma;
+  if (lo < 0.0) lo = 0.0;
+  double hi = r + gamma;
+  if (hi > 1.0) hi = 1.0;
+  pop_counts c;
+  c.n_P = static_cast<int>(round_half_even(lo * N));
+  c.n_R = N - static_cast<int>(round_half_even(hi * N));
+  c.keep = N - static_cast<int>(round_half_even(r * N));
+  c.k = c.keep - c.n_R;
+  c.n_C = N - c.n_P - c.n_R;
+  if (c.k < 0 || c.k > c.n_C)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_region_counts: fill count outside [0, |C|]");
+  *out = c;
+  return POP_OK;
+}
+
+pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1, const void* W2, void* stream,
+                          pop_ffn_t* out) {
+  if (!out) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: out is NULL");
+  *out = nullptr;
+  if (!cfg || !Wg || !W1 || !W2) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: NULL argument");
+  if (cfg->D < 8 || cfg->D > POP_MAX_D || cfg->D % 8 != 0)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: D must be a multiple of 8 in [8, POP_MAX_D]");
+  if (cfg->D_FF < 1 || cfg->D_FF > POP_MAX_D_FF)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: D_FF must be in [1, POP_MAX_D_FF]");
+  if (cfg->period < 1) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: period must be >= 1");
+  if (cfg->max_batch < 1 || cfg->max_batch > POP_MAX_BATCH)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: max_batch must be in [1, POP_MAX_BATCH]");
+  if (cfg->max_prefill_tokens < 1)
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: max_prefill_tokens must be >= 1");
+  if (!aligned16(Wg) || !aligned16(W1) || !aligned16(W2))
+    return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: weights must be 16-byte aligned");
+  pop_counts cnt;
+  pop_status s = pop_region_counts(cfg->D_FF, cfg->r, cfg->gamma, &cnt);
+  if (s != POP_OK) return s;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(nullptr, POP_ERR_UNSUPPORTED, "pop_ffn_create: this build targets sm_103a (GB300) only");
+
+  pop_ffn* h = new pop_ffn();
+  h->cfg = *cfg;
+  h->cnt = cnt;
+  h->D = cfg->D;
+  h->N = cfg->D_FF;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  const int D = h->D, N = h->N;
+  h->Mcap = round_up(cfg->max_prefill_tokens, 128);
+  h->ldZ = round_up(N, 128);
+  h->ldPart = h->ldZ;
+  const int gk = down_decode_parts(D, 2, 1 << 30, h->num_sms);
+  h->ypart_parts = std::max(h->num_sms, gk * cfg->max_batch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  auto bail = [&](cudaError_t err, const char* where) {
+    free_all(h);
+    delete h;
+    return cuda_fail(nullptr, err, where);
+  };
+#define POP_ALLOC(ptr, count)                                   \
+  do {                                                          \
+    cudaError_t e_ = dalloc(&(ptr), (count));                   \
+    if (e_ != cudaSuccess) return bail(e_, "cudaMalloc " #ptr); \
+  } while (0)
+  POP_ALLOC(h->Wp, static_cast<size_t>(N) * 3 * D);
+  POP_ALLOC(h->n2, N);
+  POP_ALLOC(h->Z, static_cast<size_t>(h->Mcap) * h->ldZ);
+  POP_ALLOC(h->part, static_cast<size_t>(h->Mcap / 32) * h->ldPart);
+  POP_ALLOC(h->sumsq, N);
+  POP_ALLOC(h->I, N);
+  POP_ALLOC(h->rc, N);
+  POP_ALLOC(h->P, N);
+  POP_ALLOC(h->idx_all, N);
+  POP_ALLOC(h->z, static_cast<size_t>(cfg->max_batch) * N);
+  POP_ALLOC(h->scores, N);
+  POP_ALLOC(h->memory, N);
+  POP_ALLOC(h->S, N);
+  POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
+  POP_ALLOC(h->step, 1);
+  POP_ALLOC(h->err, 1);
+#undef POP_ALLOC
+  if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  // index lists always hold valid positions, even before the first partition or selection
+  if ((e = cudaMemsetAsync(h->S, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  if ((e = cudaMemsetAsync(h->rc, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  k_iota<<<(N + 255) / 256, 256, 0, st>>>(h->idx_all, N);
+  if ((e = cudaGetLastError()) != cudaSuccess) return bail(e, "k_iota");
+  if ((e = launch_pack(static_cast<const uint16_t*>(Wg), static_cast<const uint16_t*>(W1),
+                       static_cast<const uint16_t*>(W2), h->Wp, h->n2, D, N, st)) != cudaSuccess)
+    return bail(e, "launch_pack");
+  if (!encode_weight_maps(&h->maps, h->Wp, D, N)) {
+    free_all(h);
+    delete h;
+    return fail(nullptr, POP_ERR_CUDA, "pop_ffn_create: cuTensorMapEncodeTiled failed");
+  }
+  *out = h;
+  return POP_OK;
+}
+
+void pop_ffn_destroy(pop_ffn_t h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+pop_status pop_ffn_counts(pop_ffn_t h, pop_counts* out) {
+  if (!h || !out) return fail(h, POP_ERR_INVALID_ARG, "pop_ffn_counts: NULL argument");
+  *out = h->cnt;
+  return POP_OK;
+}
+
+pop_status pop_set_wait_limit(pop_ffn_t h, uint64_t ns) {
+  if (!h || ns == 0) return fail(h, POP_ERR_INVALID_ARG, "pop_set_wait_limit: NULL handle or zero limit");
+  h->wait_ns = ns;
+  return POP_OK;
+}
+
+// Dense gate/up + down over M tokens through the tensor-core GEMMs (chunks of Mcap tokens).
+// When `fold` is set, the channel sums of z^2 are accumulated into h->sumsq.
+static pop_status prefill_gemms(pop_ffn* h, const uint16_t* X, int M, void* Y, bool fold, cudaStream_t st) {
+  const size_t esz = h->cfg.out_f32 ? 4 : 2;
+  for (int c0 = 0; c0 < M; c0 += h->Mcap) {
+    const int Mc = std::min(h->Mcap, M - c0);
+    CUtensorMap xm, zm;
+    if (!encode_x_map(&xm, X + static_cast<size_t>(c0) * h->D, Mc, h->D) ||
+        !encode_z_map(&zm, h->Z, Mc, h->N, h->ldZ))
+      return fail(h, POP_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    POP_CUDA(h, launch_prefill_gateup(xm, h->maps, Mc, h->N, h->D, h->Z, h->ldZ, h->part, h->ldPart, h->err,
+                                      h->wait_ns, h->num_sms, st));
+    if (fold)
+      POP_CUDA(h, launch_fold_sumsq(h->part, 4 * ((Mc + 127) / 128), h->ldPart, h->N, h->sumsq, c0 > 0 ? 1 : 0, st));
+    if (Y)
+      POP_CUDA(h, launch_prefill_down(zm, h->maps, Mc, h->N, h->D,
+                                      static_cast<uint8_t*>(Y) + static_cast<size_t>(c0) * h->D * esz,
+                                      h->cfg.out_f32, h->err, h->wait_ns, h->num_sms, st));
+  }
+  return POP_OK;
+}
+
+pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, void* stream) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_prefill_partition: NULL handle");
+  if (!X || M < 1) return fail(h, POP_ERR_INVALID_ARG, "pop_prefill_partition: X is NULL or M < 1");
+  if (!aligned16(X) || (Y && !aligned16(Y)))
+    return fail(h, POP_ERR_INVALID_ARG, "pop_prefill_partition: X and Y must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pop_status s = prefill_gemms(h, static_cast<const uint16_t*>(X), M, Y, true, st);
+  if (s != POP_OK) return s;
+  POP_CUDA(h, launch_partition(h->sumsq, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step,
+                               h->memory, h->err, st));
+  h->partitioned = true;
+  h->selected = false;
+  return POP_OK;
+}
+
+pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, void* stream) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_partition_from_importance: NULL handle");
+  if (!importance) return fail(h, POP_ERR_INVALID_ARG, "pop_partition_from_importance: NULL importance");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  POP_CUDA(h, cudaMemcpyAsync(h->I, importance, sizeof(float) * h->N, cudaMemcpyDeviceToDevice, st));
+  POP_CUDA(h, launch_partition(nullptr, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step, h->memory,
+                               h->err, st));
+  h->partitioned = true;
+  h->selected = false;
+  return POP_OK;
+}
+
+pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int* P, void* stream) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_set_partition: NULL handle");
+  const int N = h->N, nR = h->cnt.n_R, nC = h->cnt.n_C, nP = h->cnt.n_P;
+  if ((nR && !R) || (nC && !C) || (nP && !P)) return fail(h, POP_ERR_INVALID_ARG, "pop_set_partition: NULL list");
+  std::vector<char> seen(N, 0);
+  auto check = [&](const int* a, int n) {
+    for (int i = 0; i < n; ++i) {
+      if (a[i] < 0 || a[i] >= N || seen[a[i]] || (i > 0 && a[i] <= a[i - 1])) return false;
+      seen[a[i]] = 1;
+    }
+    return true;
+  };
+  if (!check(R, nR) || !check(C, nC) || !check(P, nP))
+    return fail(h, POP_ERR_INVALID_ARG, "pop_set_partition: lists must be ascending, disjoint and in [0, D_FF)");
+  std::vector<int> rc(static_cast<size_t>(nC) + nR);
+  if (nC) std::memcpy(rc.data(), C, sizeof(int) * nC);
+  if (nR) std::memcpy(rc.data() + nC, R, sizeof(int) * nR);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!rc.empty())
+    POP_CUDA(h, cudaMemcpyAsync(h->rc, rc.data(), sizeof(int) * rc.size(), cudaMemcpyHostToDevice, st));
+  if (nP) POP_CUDA(h, cudaMemcpyAsync(h->P, P, sizeof(int) * nP, cudaMemcpyHostToDevice, st));
+  POP_CUDA(h, cudaMemsetAsync(h->step, 0, sizeof(int), st));
+  POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
+  POP_CUDA(h, cudaStreamSynchronize(st));
+  h->partitioned = true;
+  h->selected = false;
+  return POP_OK;
+}
+
+pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* stream) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_decode_step: NULL handle");
+  if (!x || !y) return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: NULL x or y");
+  if (B < 1 || B > h->cfg.max_batch)
+    return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: B outside [1, max_batch]");
+  if (!aligned16(x) || !aligned16(y))
+    return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: x, y must be 16-byte aligned");
+  if (!h->partitioned) return fail(h, POP_ERR_STATE, "pop_decode_step: no partition (run a prefill first)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const PackedWeights w = packed(h);
+  const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
+  POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
+                                   h->err, h->num_sms, st));
+  POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+  int G = 0;
+  POP_CUDA(h, launch_down_decode(w, h->rc, nC, nR, h->S, h->cnt.k, h->z, nRC, B, h->ypart,
+                                 h->ypart_parts / (B == 1 ? 1 : B), &G, h->err, h->num_sms, st));
+  POP_CUDA(h, launch_reduce_y(h->ypart, G, B, h->D, y, h->cfg.out_f32, st));
+  h->selected = true;
+  return POP_OK;
+}
+
+pop_status pop_ffn_dense_ref(pop_ffn_t h, const void* X, int M, void* Y, void* stream) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_dense_ref: NULL handle");
+  if (!X || !Y || M < 1) return fail(h, POP_ERR_INVALID_ARG, "pop_ffn_dense_ref: NULL X/Y or M < 1");
+  if (!aligned16(X) || !aligned16(Y))
+    return fail(h, POP_ERR_INVALID_ARG, "pop_ffn_dense_ref: X, Y must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M > h->cfg.max_batch) return prefill_gemms(h, static_cast<const uint16_t*>(X), M, Y, false, st);
+  const PackedWeights w = packed(h);
+  POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, h->z, h->N, h->scores,
+                                   h->err, h->num_sms, st));
+  int G = 0;
+  POP_CUDA(h, launch_down_decode(w, h->idx_all, 0, h->N, h->S, 0, h->z, h->N, M, h->ypart,
+                                 h->ypart_parts / (M == 1 ? 1 : M), &G, h->err, h->num_sms, st));
+  POP_CUDA(h, launch_reduce_y(h->ypart, G, M, h->D, Y, h->cfg.out_f32, st));
+  return POP_OK;
+}
+
+pop_status pop_get_partition(pop_ffn_t h, int* R, int* C, int* P) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_get_partition: NULL handle");
+  if (!h->partitioned) return fail(h, POP_ERR_STATE, "pop_get_partition: no partition yet");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  const int nC = h->cnt.n_C, nR = h->cnt.n_R, nP = h->cnt.n_P;
+  if (C && nC) POP_CUDA(h, cudaMemcpy(C, h->rc, sizeof(int) * nC, cudaMemcpyDeviceToHost));
+  if (R && nR) POP_CUDA(h, cudaMemcpy(R, h->rc + nC, sizeof(int) * nR, cudaMemcpyDeviceToHost));
+  if (P && nP) POP_CUDA(h, cudaMemcpy(P, h->P, sizeof(int) * nP, cudaMemcpyDeviceToHost));
+  return POP_OK;
+}
+
+pop_status pop_get_importance(pop_ffn_t h, float* importance, float* sumsq) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_get_importance: NULL handle");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  if (importance) POP_CUDA(h, cudaMemcpy(importance, h->I, sizeof(float) * h->N, cudaMemcpyDeviceToHost));
+  if (sumsq) POP_CUDA(h, cudaMemcpy(sumsq, h->sumsq, sizeof(float) * h->N, cudaMemcpyDeviceToHost));
+  return POP_OK;
+}
+
+pop_status pop_get_selected(pop_ffn_t h, int* k_out, int* channels) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_get_selected: NULL handle");
+  if (!h->selected) return fail(h, POP_ERR_STATE, "pop_get_selected: no decode step since the partition was set");
+  if (k_out) *k_out = h->cnt.k;
+  if (!channels || h->cnt.k == 0) return POP_OK;
+  POP_CUDA(h, cudaDeviceSynchronize());
+  std::vector<int> S(h->cnt.k), C(h->cnt.n_C);
+  POP_CUDA(h, cudaMemcpy(S.data(), h->S, sizeof(int) * S.size(), cudaMemcpyDeviceToHost));
+  POP_CUDA(h, cudaMemcpy(C.data(), h->rc, sizeof(int) * C.size(), cudaMemcpyDeviceToHost));
+  for (int j = 0; j < h->cnt.k; ++j) {
+    if (S[j] < 0 || S[j] >= h->cnt.n_C) return fail(h, POP_ERR_DEVICE, "pop_get_selected: position out of range");
+    channels[j] = C[S[j]];
+  }
+  return POP_OK;
+}
+
+pop_status pop_get_scores(pop_ffn_t h, float* scores, float* memory) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_get_scores: NULL handle");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  const int nC = h->cnt.n_C;
+  if (scores && nC) POP_CUDA(h, cudaMemcpy(scores, h->scores, sizeof(float) * nC, cudaMemcpyDeviceToHost));
+  if (memory && nC) POP_CUDA(h, cudaMemcpy(memory, h->memory, sizeof(float) * nC, cudaMemcpyDeviceToHost));
+  return POP_OK;
+}
+
+pop_status pop_get_step(pop_ffn_t h, int* step) {
+  if (!h || !step) return fail(h, POP_ERR_INVALID_ARG, "pop_get_step: NULL argument");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  POP_CUDA(h, cudaMemcpy(step, h->step, sizeof(int), cudaMemcpyDeviceToHost));
+  return POP_OK;
+}
+
+pop_status pop_check(pop_ffn_t h) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_check: NULL handle");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  unsigned e = 0;
+  POP_CUDA(h, cudaMemcpy(&e, h->err, sizeof(unsigned), cudaMemcpyDeviceToHost));
+  if (e == 0) return POP_OK;
+  POP_CUDA(h, cudaMemset(h->err, 0, sizeof(unsigned)));
+  char buf[200];
+  std::snprintf(buf, sizeof buf,
+                "device error word 0x%x (1/2: gate-up/down wait ran out; 4: partition; 8: top-k; 16: index)", e);
+  return fail(h, (e & DEVERR_TIMEOUT_ANY) ? POP_ERR_TIMEOUT : POP_ERR_DEVICE, buf);
+}
+
+}  // extern "C"
