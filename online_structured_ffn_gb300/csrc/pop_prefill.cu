@@ -34,6 +34,10 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
 constexpr int GU_BN = 128;           // channels per gate/up tile
 constexpr int DN_BN = 256;           // outputs per down tile
+// Limit for the waits that drain a CTA's own copies and MMAs before it frees TMEM and exits;
+// independent of the caller's wait limit so that a short limit never lets a CTA exit with work
+// of its own in flight.
+constexpr uint64_t DRAIN_NS = 1000000000ull;
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t lo = issued > STAGES ? issued - STAGES : 0;
       for (uint32_t u = lo; u < issued; ++u) {
         volatile int never = 0;
-        if (!mbar_wait_bounded(&ctl->full[u % STAGES], (u / STAGES) & 1u, wait_ns, &never)) fail();
+        if (!mbar_wait_bounded(&ctl->full[u % STAGES], (u / STAGES) & 1u, DRAIN_NS, &never)) fail();
       }
     }
     __syncwarp();
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // all MMAs issued by this thread must finish before TMEM is freed
       umma_commit(&ctl->drain);
       volatile int never = 0;
-      if (!mbar_wait_bounded(&ctl->drain, 0, wait_ns, &never)) fail();
+      if (!mbar_wait_bounded(&ctl->drain, 0, DRAIN_NS, &never)) fail();
     }
     __syncwarp();
   } else {

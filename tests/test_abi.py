@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol include/pop_ffn.h declares,
+and its host-side logic (region counts, argument checks) agrees with the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pop():
+    import __graft_entry__
+    __graft_entry__.build()
+    import online_structured_ffn_gb300 as pop
+    return pop
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "pop_ffn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pop_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(pop):
+    names = _declared_functions()
+    assert len(names) >= 18
+    lib = ctypes.CDLL(pop.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pop_ffn.h but not exported"
+    assert set(names) == set(pop.SIGNATURES), "binding and header disagree"
+
+
+def test_library_is_sm103a_build(pop):
+    # the build step compiles for exactly one target; the shared object must exist in-tree
+    assert os.path.exists(pop.LIB_PATH)
+    assert os.path.dirname(pop.LIB_PATH).endswith("online_structured_ffn_gb300")
+
+
+@pytest.mark.parametrize("N", [0, 1, 7, 100, 1000, 1024, 11008, 14336, 28672, 49152])
+@pytest.mark.parametrize("r,gamma", [(0.3, 0.1), (0.299, 0.1), (0.5, 0.1), (0.0, 0.1), (0.3, 0.0), (0.4, 0.6),
+                                     (1.0, 0.1), (0.25, 0.05), (0.125, 0.125)])
+def test_region_counts_match_oracle(pop, N, r, gamma):
+    ref = oracle.region_counts(N, r, gamma)
+    got = pop.pop_region_counts(N, r, gamma)
+    assert (got.n_P, got.n_R, got.n_C, got.keep, got.k) == (ref.n_P, ref.n_R, ref.n_C, ref.keep, ref.k)
+
+
+def test_region_counts_rejects_bad_args(pop):
+    for N, r, g in [(10, -0.1, 0.1), (10, 1.1, 0.1), (10, 0.3, -0.5), (-1, 0.3, 0.1)]:
+        with pytest.raises(pop.PopError) as e:
+            pop.pop_region_counts(N, r, g)
+        assert e.value.status == pop.POP_ERR_INVALID_ARG
+    assert pop.load_library().pop_region_counts(10, 0.3, 0.1, None) == pop.POP_ERR_INVALID_ARG
+
+
+def test_create_rejects_bad_config_before_touching_cuda(pop):
+    lib = pop.load_library()
+    out = ctypes.c_void_p(1)
+    good = dict(D=256, D_FF=1024, r=0.3, gamma=0.1, period=1, max_batch=1, max_prefill_tokens=64, out_f32=1)
+    fake = 4096  # any 16-byte aligned non-null value: the checks below fail before it is used
+    bad = [dict(D=100), dict(D=0), dict(D=20000), dict(D_FF=0), dict(D_FF=60000), dict(period=0),
+           dict(max_batch=0), dict(max_batch=65), dict(max_prefill_tokens=0), dict(r=1.5), dict(gamma=-1.0)]
+    for b in bad:
+        cfg = pop.pop_config(**{**good, **b})
+        assert lib.pop_ffn_create(ctypes.byref(cfg), fake, fake, fake, None, ctypes.byref(out)) == \
+            pop.POP_ERR_INVALID_ARG, b
+        assert out.value is None
+        assert lib.pop_last_error(None)
+    cfg = pop.pop_config(**good)
+    assert lib.pop_ffn_create(ctypes.byref(cfg), None, fake, fake, None, ctypes.byref(out)) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_ffn_create(ctypes.byref(cfg), fake + 2, fake, fake, None, ctypes.byref(out)) == \
+        pop.POP_ERR_INVALID_ARG  # misaligned
+    assert lib.pop_ffn_create(None, fake, fake, fake, None, ctypes.byref(out)) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_ffn_create(ctypes.byref(cfg), fake, fake, fake, None, None) == pop.POP_ERR_INVALID_ARG
+
+
+def test_null_handle_calls(pop):
+    lib = pop.load_library()
+    assert lib.pop_prefill_partition(None, 4096, 1, None, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_decode_step(None, 4096, 1, 4096, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_ffn_dense_ref(None, 4096, 1, 4096, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_check(None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_set_wait_limit(None, 5) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_get_partition(None, None, None, None) == pop.POP_ERR_INVALID_ARG
+    assert b"NULL" in lib.pop_last_error(None)
+    lib.pop_ffn_destroy(None)  # no-op
+
+
+def test_status_strings(pop):
+    lib = pop.load_library()
+    for s in range(8):
+        assert lib.pop_status_string(s).decode() == pop.status_name(s)
+    assert lib.pop_status_string(99) == b"POP_ERR_UNKNOWN"

@@ -1,0 +1,106 @@
+"""Parity at the workload sizes, in the launch configuration the benchmark uses.
+
+LLaMA-2-7B FFN shape (D=4096, D_FF=11008) with B=1 and B=16, and the LLaMA-70B FFN shape
+(D=8192, D_FF=28672) with B=64 and a period of 16. A full CPU prefill at these sizes is out of
+reach for the float64 oracle, so prefill is checked on sampled channels and tokens, plus the
+property that the GPU's R/C/P split is the counting rule applied to its own importance; decode
+steps are checked in full on a partition the oracle computes from a short prompt.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import parity
+
+pytestmark = pytest.mark.gpu
+
+f64 = synth.bf16_to_f64
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import online_structured_ffn_gb300 as pop
+    torch.cuda.set_device(0)
+    return pop, torch, torch.device("cuda", 0)
+
+
+def up(env, a):
+    _, torch, dev = env
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def _layer(env, D, N, **kw):
+    pop = env[0]
+    Wg, W1, W2 = synth.ffn_weights(0, D, N)
+    ffn = pop.PopFFN(up(env, Wg), up(env, W1), up(env, W2), **kw)
+    return ffn, (Wg, W1, W2), synth.dim_scales(0, D)
+
+
+def test_prefill_7b_sampled(env):
+    _, torch, dev = env
+    D, N, L = 4096, 11008, 2048
+    ffn, (Wg, W1, W2), sc = _layer(env, D, N, r=0.299, gamma=0.1, max_batch=1, max_prefill_tokens=L)
+    X = synth.prompt(0, L, sc)
+    Y = torch.empty((L, D), dtype=torch.float32, device=dev)
+    ffn.prefill_partition(up(env, X), Y)
+    ffn.check()
+    I, ss = ffn.importance()
+    rng = np.random.default_rng(0)
+    ch = np.sort(rng.choice(N, 96, replace=False))
+    Xf = f64(X)
+    Z = oracle.ffn_activations(f64(Wg[ch]), f64(W1[ch]), Xf)
+    ss_ref, I_ref = oracle.channel_importance(f64(W2[:, ch]), Z)
+    assert np.all(np.abs(ss[ch] - ss_ref) <= 1e-4 * ss_ref + 1e-7 * ss_ref.max())
+    assert np.all(np.abs(I[ch] - I_ref) <= 1e-4 * I_ref + 1e-7 * I_ref.max())
+    rows = np.sort(rng.choice(L, 4, replace=False))
+    Zr = oracle.ffn_activations(f64(Wg), f64(W1), Xf[rows])
+    Yr = oracle.down_projection(f64(W2), Zr)
+    Yg = Y.cpu().numpy()[rows]
+    assert parity.rel_l2(Yg, Yr) <= parity.Y_REL_L2
+    assert np.all(np.abs(Yg - Yr) <= 2.0 ** -8 * (np.abs(Zr) @ np.abs(f64(W2)).T) + 1e-6)
+    # property at full size: the split is the counting rule applied to the GPU's own importance
+    R, C, P = ffn.partition()
+    R0, C0, P0 = oracle.partition(I, oracle.region_counts(N, 0.299, 0.1))
+    assert np.array_equal(R, R0) and np.array_equal(C, C0) and np.array_equal(P, P0)
+    ffn.close()
+
+
+def _decode(env, ffn, W, sc, r, gamma, B, steps, period=1, prompt_len=8):
+    Wg, W1, W2 = (f64(w) for w in W)
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, prompt_len, sc)), r, gamma)
+    ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], ref["counts"].k, period=period)
+    checked = 0
+    for t in range(steps):
+        x = synth.decode_input(0, t, B, sc)
+        mem_before = sess.memory.copy()
+        y = ffn.decode_step(up(env, x)).cpu().numpy()
+        y_ref = sess.step(f64(x))
+        if t % period == 0:
+            used = mem_before + sess.last_scores
+            bad, _, nd = parity.compare_selection(ffn.selected(), sess.C[sess.S], sess.C, used, ref["counts"].k)
+            assert not bad, f"step {t}: selection differs outside the flagged band"
+            if nd:
+                continue
+        parity.check_y(y, y_ref, f"B={B} step {t}")
+        checked += 1
+    ffn.check()
+    assert checked >= 1
+
+
+@pytest.mark.parametrize("B,r", [(1, 0.299), (16, 0.5)])
+def test_decode_7b(env, B, r):
+    ffn, W, sc = _layer(env, 4096, 11008, r=r, gamma=0.1, max_batch=B, max_prefill_tokens=2048)
+    _decode(env, ffn, W, sc, r, 0.1, B, steps=3)
+    ffn.close()
+
+
+def test_decode_70b_b64_periodic(env):
+    ffn, W, sc = _layer(env, 8192, 28672, r=0.5, gamma=0.1, period=16, max_batch=64, max_prefill_tokens=512)
+    _decode(env, ffn, W, sc, 0.5, 0.1, 64, steps=2, period=16, prompt_len=4)
+    ffn.close()

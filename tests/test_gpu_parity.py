@@ -1,0 +1,298 @@
+"""GPU parity: the sm_103a library, called through its C ABI, against the CPU oracle.
+
+Sets must match exactly outside the flagged band (oracle score within 1e-4 relative of a
+cut-off); decode outputs within rel-L2 5e-3 and max-abs 2e-2. Prefill Y is the one output made
+from a bf16 operand (Z is rounded to bf16 as the A operand of the down GEMM), so it is held to
+the rounding bound that step implies: |Y - Y_ref| <= 2^-8 * (|Z| |W2|^T) per element, plus the
+rel-L2 bound.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import online_structured_ffn_gb300 as pop
+    torch.cuda.set_device(0)
+    return pop, torch, torch.device("cuda", 0)
+
+
+def up(env, a):
+    pop, torch, dev = env
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+f64 = synth.bf16_to_f64
+
+
+class Layer:
+    def __init__(self, env, D, N, seed=0, **kw):
+        self.D, self.N, self.seed = D, N, seed
+        self.Wg, self.W1, self.W2 = synth.ffn_weights(seed, D, N)
+        self.sc = synth.dim_scales(seed, D)
+        self.env = env
+        pop = env[0]
+        self.ffn = pop.PopFFN(up(env, self.Wg), up(env, self.W1), up(env, self.W2), **kw)
+        self.counts = self.ffn.counts
+
+    def w64(self):
+        return f64(self.Wg), f64(self.W1), f64(self.W2)
+
+    def close(self):
+        self.ffn.close()
+
+
+def _prefill_y_bound(Wg, W1, W2, X):
+    Z = oracle.ffn_activations(Wg, W1, X)
+    return 2.0 ** -8 * (np.abs(Z) @ np.abs(W2).T) + 1e-6
+
+
+SHAPES = [  # D, N, L, r, gamma, max_prefill_tokens
+    (256, 1024, 64, 0.3, 0.1, 64),        # tiny single layer
+    (264, 1000, 77, 0.3, 0.1, 77),        # ragged D (not a multiple of 64), N, M
+    (256, 1024, 300, 0.5, 0.1, 128),      # prompt longer than one prefill chunk
+    (1024, 4096, 512, 0.299, 0.1, 512),   # several tiles in every dimension
+    (512, 2000, 1, 0.3, 0.1, 16),         # one prompt token
+]
+
+
+@pytest.mark.parametrize("D,N,L,r,gamma,maxM", SHAPES)
+def test_prefill_partition(env, D, N, L, r, gamma, maxM):
+    lay = Layer(env, D, N, r=r, gamma=gamma, max_prefill_tokens=maxM)
+    _, torch, dev = env
+    X = synth.prompt(lay.seed, L, lay.sc)
+    Y = torch.empty((L, D), dtype=torch.float32, device=dev)
+    lay.ffn.prefill_partition(up(env, X), Y)
+    lay.ffn.check()
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(X), r, gamma)
+    Yg = Y.cpu().numpy()
+    assert parity.rel_l2(Yg, ref["Y"]) <= parity.Y_REL_L2
+    assert np.all(np.abs(Yg - ref["Y"]) <= _prefill_y_bound(Wg, W1, W2, f64(X)))
+    I, ss = lay.ffn.importance()
+    assert np.all(np.abs(ss - ref["ss"]) <= 1e-4 * ref["ss"] + 1e-7 * ref["ss"].max())
+    assert np.all(np.abs(I - ref["I"]) <= 1e-4 * ref["I"] + 1e-7 * ref["I"].max())
+    bad, nflag, ndiff = parity.compare_partition(lay.ffn.partition(), (ref["R"], ref["C"], ref["P"]), ref["I"],
+                                                 ref["counts"])
+    assert len(bad) == 0, f"partition differs outside the flagged band ({nflag} flagged): {bad[:8]}"
+    assert lay.ffn.step_count() == 0
+    lay.close()
+
+
+@pytest.mark.parametrize("N,r,gamma", [(1, 0.3, 0.1), (7, 0.5, 0.2), (1000, 0.3, 0.1), (11008, 0.299, 0.1),
+                                       (28672, 0.5, 0.1), (49152, 0.3, 0.1), (4096, 0.0, 0.1), (4096, 0.3, 0.0),
+                                       (4096, 0.4, 0.6), (4096, 1.0, 0.1)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_partition_from_importance_is_exact(env, N, r, gamma, ties):
+    # same float32 keys on both sides: the selection must be identical, ties included
+    _, torch, dev = env
+    D = 64
+    lay = Layer(env, D, N, r=r, gamma=gamma)
+    rng = np.random.default_rng(N)
+    I = rng.integers(0, 12, size=N).astype(np.float32) * 0.5 if ties else rng.random(N).astype(np.float32)
+    lay.ffn.partition_from_importance(torch.from_numpy(I).to(dev))
+    lay.ffn.check()
+    R, C, P = lay.ffn.partition()
+    R0, C0, P0 = oracle.partition(I, oracle.region_counts(N, r, gamma))
+    assert np.array_equal(R, R0) and np.array_equal(C, C0) and np.array_equal(P, P0)
+    lay.close()
+
+
+def _decode_session(env, lay, ref_part, B, steps):
+    """Per-step POP on the oracle's partition; returns how many flagged near-ties flipped."""
+    Wg, W1, W2 = lay.w64()
+    R, C, P = ref_part
+    lay.ffn.set_partition(R, C, P)
+    sess = oracle.PopSession(Wg, W1, W2, R, C, lay.counts.k)
+    flips = 0
+    for t in range(steps):
+        x = synth.decode_input(lay.seed, t, B, lay.sc)
+        y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+        y_ref = sess.step(f64(x))
+        if lay.counts.n_C:
+            a, _ = lay.ffn.scores()
+            amax = sess.last_scores.max()
+            assert np.all(np.abs(a - sess.last_scores) <= 1e-3 * sess.last_scores + 1e-5 * amax)
+        if lay.counts.k:
+            bad, _, nd = parity.compare_selection(lay.ffn.selected(), sess.C[sess.S], sess.C, sess.last_scores,
+                                                  lay.counts.k)
+            assert not bad, f"step {t}: selection differs outside the flagged band: {bad[:8]}"
+            flips += nd
+            if nd:
+                continue  # a flagged near-tie flipped: y is built on a different, equally valid set
+        parity.check_y(y, y_ref, f"B={B} step {t}")
+    assert lay.ffn.step_count() == steps
+    lay.ffn.check()
+    return flips
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 8, 16, 33, 64])
+def test_decode_parity(env, B):
+    D, N, r, gamma = 512, 2048, 0.3, 0.1
+    lay = Layer(env, D, N, r=r, gamma=gamma, max_batch=B)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 32, lay.sc)), r, gamma)
+    _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), B, steps=4)
+    lay.close()
+
+
+@pytest.mark.parametrize("D,N", [(264, 1000), (1024, 4096), (4096, 1100)])
+def test_decode_parity_shapes(env, D, N):
+    lay = Layer(env, D, N, r=0.299, gamma=0.1, max_batch=16)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 16, lay.sc)), 0.299, 0.1)
+    for B in (1, 16):
+        _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), B, steps=3)
+    lay.close()
+
+
+@pytest.mark.parametrize("period,B", [(4, 1), (4, 4), (16, 2)])
+def test_periodic_memory(env, period, B):
+    D, N, r, gamma = 256, 1024, 0.5, 0.1
+    lay = Layer(env, D, N, r=r, gamma=gamma, period=period, max_batch=B)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 64, lay.sc)), r, gamma)
+    lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k, period=period)
+    held = None
+    for t in range(2 * period + 3):
+        x = synth.decode_input(0, t, B, lay.sc)
+        y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+        # the oracle's memory just before this step's update is what the selection used
+        mem_before = sess.memory.copy()
+        y_ref = sess.step(f64(x))
+        S = lay.ffn.selected()
+        if t % period == 0:
+            used = mem_before + sess.last_scores
+            bad, _, nd = parity.compare_selection(S, sess.C[sess.S], sess.C, used, lay.counts.k)
+            assert not bad
+            held = S.copy()
+            if nd == 0:
+                parity.check_y(y, y_ref, f"periodic step {t}")
+        else:
+            assert np.array_equal(S, held), "selection must be held between updates"
+            a, mem = lay.ffn.scores()
+            amax = max(sess.last_scores.max(), 1e-30)
+            assert np.all(np.abs(mem - sess.memory) <= 1e-4 * np.abs(sess.memory) + 1e-5 * amax)
+            if set(held.tolist()) == set(sess.C[sess.S].tolist()):
+                parity.check_y(y, y_ref, f"periodic step {t}")
+    lay.ffn.check()
+    lay.close()
+
+
+def test_period_one_equals_per_step(env):
+    D, N = 256, 1024
+    a = Layer(env, D, N, r=0.5, gamma=0.1, period=1)
+    b = Layer(env, D, N, r=0.5, gamma=0.1, period=1)
+    Wg, W1, W2 = a.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 16, a.sc)), 0.5, 0.1)
+    for lay in (a, b):
+        lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    for t in range(3):
+        x = up(env, synth.decode_input(0, t, 1, a.sc))
+        ya = a.ffn.decode_step(x).cpu().numpy()
+        yb = b.ffn.decode_step(x).cpu().numpy()
+        assert np.array_equal(ya, yb)  # the library is deterministic run to run
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 200])
+def test_dense_ref(env, M):
+    D, N = 512, 2000
+    lay = Layer(env, D, N, r=0.3, gamma=0.1, max_batch=16, max_prefill_tokens=128)
+    X = synth.prompt(0, M, lay.sc)
+    Wg, W1, W2 = lay.w64()
+    Y = lay.ffn.dense_ref(up(env, X)).cpu().numpy()
+    Yr = oracle.dense_ffn(Wg, W1, W2, f64(X))
+    if M <= 16:
+        parity.check_y(Y, Yr, f"dense M={M}")
+    else:
+        assert parity.rel_l2(Y, Yr) <= parity.Y_REL_L2
+        assert np.all(np.abs(Y - Yr) <= _prefill_y_bound(Wg, W1, W2, f64(X)))
+    lay.ffn.check()
+    lay.close()
+
+
+def test_rate_zero_is_dense_on_gpu(env):
+    D, N = 512, 2048
+    lay = Layer(env, D, N, r=0.0, gamma=0.1, max_batch=4)
+    assert lay.counts.k == lay.counts.n_C and lay.counts.keep == N
+    _, torch, dev = env
+    lay.ffn.prefill_partition(up(env, synth.prompt(0, 32, lay.sc)))
+    for B in (1, 4):
+        x = up(env, synth.decode_input(0, 0, B, lay.sc))
+        y = lay.ffn.decode_step(x).cpu().numpy()
+        yd = lay.ffn.dense_ref(x).cpu().numpy()
+        assert parity.rel_l2(y, yd) <= 1e-5
+    lay.close()
+
+
+def test_gamma_zero_and_full_reevaluation(env):
+    D, N = 256, 1024
+    for r, gamma in [(0.3, 0.0), (0.4, 0.6)]:
+        lay = Layer(env, D, N, r=r, gamma=gamma)
+        Wg, W1, W2 = lay.w64()
+        ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 16, lay.sc)), r, gamma)
+        _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), 1, steps=3)
+        lay.close()
+
+
+def test_everything_pruned_gives_zero(env):
+    lay = Layer(env, 256, 512, r=1.0, gamma=0.1, max_batch=2)
+    assert lay.counts.keep == 0
+    lay.ffn.prefill_partition(up(env, synth.prompt(0, 8, lay.sc)))
+    y = lay.ffn.decode_step(up(env, synth.decode_input(0, 0, 2, lay.sc))).cpu().numpy()
+    assert np.all(y == 0.0)
+    lay.ffn.check()
+    lay.close()
+
+
+def test_bf16_output(env):
+    _, torch, dev = env
+    lay = Layer(env, 256, 1024, r=0.3, gamma=0.1, out_f32=False)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 16, lay.sc)), 0.3, 0.1)
+    lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k)
+    x = synth.decode_input(0, 0, 1, lay.sc)
+    y = lay.ffn.decode_step(up(env, x))
+    assert y.dtype == torch.bfloat16
+    parity.check_y(y.float().cpu().numpy(), sess.step(f64(x)))
+    lay.close()
+
+
+def test_state_and_argument_errors(env):
+    pop, torch, dev = env
+    lay = Layer(env, 256, 1024, r=0.3, gamma=0.1, max_batch=2)
+    x = up(env, synth.decode_input(0, 0, 1, lay.sc))
+    y = torch.empty((4, 256), dtype=torch.float32, device=dev)
+    with pytest.raises(pop.PopError) as e:
+        lay.ffn.decode_step(x, y)
+    assert e.value.status == pop.POP_ERR_STATE
+    lay.ffn.prefill_partition(up(env, synth.prompt(0, 8, lay.sc)))
+    with pytest.raises(pop.PopError) as e:
+        pop.pop_decode_step(lay.ffn.handle, x, 3, y)  # B > max_batch
+    assert e.value.status == pop.POP_ERR_INVALID_ARG
+    with pytest.raises(pop.PopError) as e:
+        pop.pop_decode_step(lay.ffn.handle, x.data_ptr() + 2, 1, y)  # misaligned
+    assert e.value.status == pop.POP_ERR_INVALID_ARG
+    c = lay.counts
+    with pytest.raises(pop.PopError) as e:  # lists that overlap
+        lay.ffn.set_partition(np.arange(c.n_R), np.arange(c.n_C), np.arange(c.n_P))
+    assert e.value.status == pop.POP_ERR_INVALID_ARG
+    with pytest.raises(pop.PopError) as e:
+        pop.pop_ffn_dense_ref(lay.ffn.handle, x, 0, y)
+    assert e.value.status == pop.POP_ERR_INVALID_ARG
+    lay.ffn.check()
+    lay.close()
