@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of the POP pruned gated-MLP FFN on GB300.
+
+One step = one full inference session of an FFN stack: prefill of every layer's prompt (dense
+FFN on the tensor cores, sum of z^2, R/C/P partition), then T decode steps that run every layer
+(gate/up over R u C, candidate top-k, down over R and the selected candidates). Default workload:
+LLaMA-2-7B FFN shape (D=4096, D_FF=11008), B=1, 2048 prompt tokens, r=0.299, gamma=0.1, 256
+decode steps, on 4 independent layer copies (1.08 GB of weights, more than 3x the 129 MB L2, so
+consecutive decode steps stream weights from HBM).
+
+value = decode tokens per second per FFN layer = B * T * layers / (session time, prefill
+included). Inputs are already in HBM when timing starts; `e2e` repeats the session through the
+same public API with inputs in pinned host memory and outputs copied back inside the timed region.
+
+`--impl reference` times the CPU oracle (float64 numpy) on the host cores instead, on a bounded
+sample of the same workload, extrapolated to the same unit.
+
+Multi-GPU (`torchrun --nproc-per-node N bench.py --gpus N`): the path has no exchange step, so
+every rank runs an independent replica; the time is the maximum over ranks and the value the
+sum of all ranks' tokens over that time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # D, D_FF, rate, gamma, batch, prompt tokens (all sequences), decode steps, period, layers, prefill chunk
+    "llama2-7b-ffn-b1": dict(D=4096, N=11008, r=0.299, gamma=0.1, B=1, M=2048, T=256, period=1, layers=4,
+                             chunk=2048),
+    "llama2-7b-ffn-b16": dict(D=4096, N=11008, r=0.5, gamma=0.1, B=16, M=16 * 1024, T=512, period=1, layers=4,
+                              chunk=4096),
+    "llama-70b-ffn-b64-p16": dict(D=8192, N=28672, r=0.5, gamma=0.1, B=64, M=64 * 512, T=1024, period=16,
+                                  layers=1, chunk=8192),
+}
+METRIC = "pruned-FFN decode tokens/s and HBM GB/s vs GB300 peak, LLaMA-7B FFN, B=1/16"
+UNIT = "tokens/s"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def touched_bytes(c, D):
+    """Algorithmic weight bytes of one decode step: gate+up rows over R u C, down columns over R u S."""
+    gateup = 2 * (c.n_R + c.n_C) * D * 2
+    down = c.keep * D * 2
+    return gateup, down
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_info():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(elapsed_s: float, units: float, device=None):
+    """Max of the elapsed times and sum of the units over all ranks (no-op with one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    def __init__(self, device_index: int):
+        import torch
+        try:
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.gpu = str(device_index)
+        self.proc = None
+        self.out = b""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        self.out = self.proc.stdout.read()
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        rows = list(csv.reader(io.StringIO(self.out.decode(errors="replace"))))
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Stack:
+    """`layers` independent POP FFN layers of one workload, with their inputs resident in HBM."""
+
+    def __init__(self, wl, seed=0):
+        import numpy as np
+        import torch
+
+        import online_structured_ffn_gb300 as pop
+        import synth
+        self.wl, self.pop, self.torch = wl, pop, torch
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
+        D, N, B, M, T, Lyr = wl["D"], wl["N"], wl["B"], wl["M"], wl["T"], wl["layers"]
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.ffn = []
+        sc = synth.dim_scales(seed, D)
+        self.X, self.Y = [], []
+        for l in range(Lyr):
+            Wg, W1, W2 = synth.ffn_weights(seed, D, N, layer=l)
+            tg, t1, t2 = up(Wg), up(W1), up(W2)
+            del Wg, W1, W2
+            f = pop.PopFFN(tg, t1, t2, r=wl["r"], gamma=wl["gamma"], period=wl["period"], max_batch=B,
+                           max_prefill_tokens=wl["chunk"], out_f32=True)
+            torch.cuda.synchronize()
+            del tg, t1, t2
+            self.ffn.append(f)
+            self.X.append(up(synth.prompt(seed, M, sc, layer=l)))
+            self.Y.append(torch.empty((M, D), dtype=torch.float32, device=dev))
+        xs = np.stack([np.stack([synth.decode_input(seed, t, B, sc, layer=l) for l in range(Lyr)])
+                       for t in range(T)])
+        self.x = up(xs)  # [T, layers, B, D]
+        self.y = torch.empty((T, Lyr, B, D), dtype=torch.float32, device=dev)
+        self.counts = self.ffn[0].counts
+        self.chunks = (M + wl["chunk"] - 1) // wl["chunk"]
+
+    def launches_per_session(self):
+        # prefill: per chunk gate/up GEMM + sum fold + down GEMM, then the partition kernel;
+        # decode: gate/up, selection, down, reduction per layer and step
+        per_layer = 3 * self.chunks + 1 + 4 * self.wl["T"]
+        return per_layer * self.wl["layers"]
+
+    def session(self, dec_events=None):
+        pop, torch = self.pop, self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        B, T = self.wl["B"], self.wl["T"]
+        for l, f in enumerate(self.ffn):
+            pop.pop_prefill_partition(f.handle, self.X[l].data_ptr(), self.X[l].shape[0], self.Y[l].data_ptr(), st)
+        if dec_events is not None:
+            dec_events[0].record()
+        handles = [f.handle for f in self.ffn]
+        lib = pop.load_library()
+        xp, yp = self.x.data_ptr(), self.y.data_ptr()
+        xstride = B * self.wl["D"] * 2
+        ystride = B * self.wl["D"] * 4
+        i = 0
+        for t in range(T):
+            for h in handles:
+                s = lib.pop_decode_step(h, xp + i * xstride, B, yp + i * ystride, st)
+                if s:
+                    pop._check(s, h)
+                i += 1
+        if dec_events is not None:
+            dec_events[1].record()
+
+    def session_e2e(self, hX, hx, hY, hy):
+        """The same session with inputs in pinned host memory, outputs copied back, all timed."""
+        pop, torch = self.pop, self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        B, T = self.wl["B"], self.wl["T"]
+        for l, f in enumerate(self.ffn):
+            self.X[l].copy_(hX[l], non_blocking=True)
+            pop.pop_prefill_partition(f.handle, self.X[l].data_ptr(), self.X[l].shape[0], self.Y[l].data_ptr(), st)
+            hY[l].copy_(self.Y[l], non_blocking=True)
+        lib = pop.load_library()
+        for t in range(T):
+            self.x[t].copy_(hx[t], non_blocking=True)
+            for l, f in enumerate(self.ffn):
+                s = lib.pop_decode_step(f.handle, self.x[t, l].data_ptr(), B, self.y[t, l].data_ptr(), st)
+                if s:
+                    pop._check(s, f.handle)
+            hy[t].copy_(self.y[t], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def close(self):
+        for f in self.ffn:
+            f.close()
+
+
+def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
+    import torch
+    wl = WORKLOADS[wl_name]
+    rank, world, local = dist_info()
+    stack = Stack(wl)
+    for f in stack.ffn:
+        f.check()
+    for _ in range(warmup):
+        stack.session()
+    torch.cuda.synchronize()
+    for f in stack.ffn:
+        f.profile(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if with_clocks else None
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__enter__()
+    ev0.record()
+    for k in range(steps):
+        stack.session(dec[k])
+    ev1.record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__()
+    barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    dec_s = sum(a.elapsed_time(b) for a, b in dec) / 1e3
+    prof = [f.profile_read() for f in stack.ffn]
+    for f in stack.ffn:
+        f.profile(False)
+        f.check()
+    B, T, Lyr = wl["B"], wl["T"], wl["layers"]
+    units = B * T * Lyr * steps
+    g_elapsed, g_units = aggregate(elapsed, units, device=torch.device("cuda", torch.cuda.current_device()))
+    ksum = [sum(p[0][i] for p in prof) for i in range(4)]
+    nsteps = sum(p[1] for p in prof)
+    c = stack.counts
+    gu_bytes, dn_bytes = touched_bytes(c, wl["D"])
+    peak, peak_kind = measured_peaks()
+    gu_ms = ksum[0] / max(nsteps, 1)
+    dec_step_s = dec_s / (T * Lyr * steps)
+    res = dict(
+        value=g_units / g_elapsed, elapsed=g_elapsed, units=g_units, ms_per_step=1e3 * g_elapsed / steps,
+        decode_only_tokens_per_s=B * T * Lyr * steps / dec_s,
+        decode_step_us=1e6 * dec_step_s,
+        prefill_ms_per_layer=1e3 * (elapsed - dec_s) / (steps * Lyr),
+        kernel_us={n: 1e3 * ksum[i] / max(nsteps, 1) for i, n in enumerate(("gateup", "select", "down", "reduce"))},
+        gateup_gbs=gu_bytes / (gu_ms * 1e-3) / 1e9,
+        peak=peak, peak_kind=peak_kind,
+        step_gbs=(gu_bytes + dn_bytes) / dec_step_s / 1e9,
+        gu_bytes=gu_bytes, dn_bytes=dn_bytes, counts=c.as_dict(),
+        launches=stack.launches_per_session() * steps,
+        clocks=sampler.summary() if sampler else None,
+    )
+    if with_e2e:
+        res["e2e"] = run_e2e(stack, max(1, min(steps, 5)))
+    stack.close()
+    del stack
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(stack, steps):
+    import torch
+    wl = stack.wl
+    hX = [x.cpu().pin_memory() for x in stack.X]
+    hY = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in stack.Y]
+    hx = stack.x.cpu().pin_memory()
+    hy = torch.empty(stack.y.shape, dtype=stack.y.dtype).pin_memory()
+    stack.session_e2e(hX, hx, hY, hy)  # warm
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        stack.session_e2e(hX, hx, hY, hy)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    barrier()
+    units = wl["B"] * wl["T"] * wl["layers"] * steps
+    g_el, g_units = aggregate(el, units, device=torch.device("cuda", torch.cuda.current_device()))
+    h2d = sum(x.numel() * x.element_size() for x in hX) + hx.numel() * hx.element_size()
+    d2h = sum(y.numel() * y.element_size() for y in hY) + hy.numel() * hy.element_size()
+    return {"value": g_units / g_el, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+class OracleSample:
+    """The CPU oracle on one layer of a workload: weights and inputs are prepared once; `run`
+    times the oracle on a bounded sample (a few prompt tokens and decode steps) and extrapolates
+    linearly to one full session of that layer (all prompt tokens, all decode steps)."""
+
+    def __init__(self, wl, seed=0, max_prefill=8, max_decode=4):
+        import oracle
+        import synth
+        self.wl, self.oracle = wl, oracle
+        f64 = synth.bf16_to_f64
+        D, N, B = wl["D"], wl["N"], wl["B"]
+        self.W = tuple(f64(w) for w in synth.ffn_weights(seed, D, N))
+        sc = synth.dim_scales(seed, D)
+        self.X = f64(synth.prompt(seed, max_prefill, sc))
+        self.xs = [f64(synth.decode_input(seed, t, B, sc)) for t in range(max_decode)]
+
+    def run(self, prefill_tokens, decode_steps):
+        wl, oracle = self.wl, self.oracle
+        Wg, W1, W2 = self.W
+        t0 = time.perf_counter()
+        pre = oracle.prefill(Wg, W1, W2, self.X[:prefill_tokens], wl["r"], wl["gamma"])
+        t_pre = time.perf_counter() - t0
+        sess = oracle.PopSession(Wg, W1, W2, pre["R"], pre["C"], pre["counts"].k, period=wl["period"])
+        t0 = time.perf_counter()
+        for x in self.xs[:decode_steps]:
+            sess.step(x)
+        t_dec = (time.perf_counter() - t0) / decode_steps
+        session = t_pre * wl["M"] / prefill_tokens + t_dec * wl["T"]
+        info = (f"one layer of the {wl['D']}x{wl['N']} FFN: oracle prefill of {prefill_tokens} of {wl['M']} "
+                f"prompt tokens ({t_pre:.2f} s) and {decode_steps} of {wl['T']} decode steps at B={wl['B']} "
+                f"({t_dec:.2f} s each), extrapolated linearly to one full session")
+        return session, info
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl):
+    session, info = OracleSample(wl).run(prefill_tokens=8, decode_steps=4)
+    return {"value": wl["B"] * wl["T"] / session, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+            "sample": info + "; float64 numpy with its default BLAS threading"}
+
+
+# ------------------------------------------------------------------ main
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = open(os.path.join(ROOT, "online_structured_ffn_gb300", "csrc", "pop_decode.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256_16")):
+            k, v = line.split(":", 1)
+            vals[k.strip().lstrip("-* ").strip("`")] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["pop", "reference"], default="pop")
+    ap.add_argument("--workload", default="llama2-7b-ffn-b1", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true", help="skip the B=16 line inside the JSON")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_info()
+    wl = WORKLOADS[args.workload]
+    config = {"workload": args.workload, "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
+              "B": wl["B"], "prompt_tokens": wl["M"], "decode_steps": wl["T"], "period": wl["period"],
+              "layers": wl["layers"],
+              "l2": "inputs larger than L2: each decode step reads another layer's weights "
+                    f"({wl['layers']} layers x {3 * wl['D'] * wl['N'] * 2 / 1e6:.0f} MB)",
+              "parallelism": "replicas" if world > 1 else "single-gpu"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        sample = OracleSample(wl, max_prefill=2, max_decode=1)
+        for _ in range(args.warmup):
+            sample.run(2, 1)
+        times, info = [], ""
+        for _ in range(args.steps):
+            s, info = sample.run(2, 1)
+            times.append(s)
+        value = wl["B"] * wl["T"] * len(times) / sum(times)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+                                 "sample": info + " (each step)"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t0}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    res = run_gpu(args.workload, args.steps, args.warmup)
+    secondary = None
+    if not args.no_secondary and args.workload == "llama2-7b-ffn-b1":
+        s = run_gpu("llama2-7b-ffn-b16", max(3, args.steps // 4), args.warmup, with_e2e=False, with_clocks=False)
+        secondary = {"workload": "llama2-7b-ffn-b16", "value": s["value"], "unit": UNIT,
+                     "decode_only_tokens_per_s": s["decode_only_tokens_per_s"],
+                     "decode_step_us": s["decode_step_us"], "kernel_us": s["kernel_us"],
+                     "gateup_hbm_gbs": s["gateup_gbs"], "gateup_frac": s["gateup_gbs"] / s["peak"],
+                     "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"]}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+    if rank != 0:
+        return
+    traffic = traffic_from_profiles("gateup_decode", args.workload)
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator)",
+        "config": config,
+        "roofline": {"bound": "hbm", "kernel": "k_gateup_b1 (decode gate/up over R u C)",
+                     "achieved": res["gateup_gbs"], "peak": res["peak"], "unit": "GB/s",
+                     "frac": res["gateup_gbs"] / res["peak"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": res["gu_bytes"], "peak_source": res["peak_kind"]},
+        "decode_step": {"us": res["decode_step_us"], "hbm_gbs": res["step_gbs"], "frac": res["step_gbs"] / res["peak"],
+                        "touched_bytes": res["gu_bytes"] + res["dn_bytes"], "kernel_us": res["kernel_us"],
+                        "tokens_per_s": res["decode_only_tokens_per_s"]},
+        "prefill_ms_per_layer": res["prefill_ms_per_layer"],
+        "counts": res["counts"],
+        "e2e": res.get("e2e"),
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+    }
+    if secondary:
+        line["secondary"] = secondary
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -155,6 +155,17 @@ pop_status pop_get_step(pop_ffn_t h, int* step);
  * A wait that runs out sets POP_ERR_TIMEOUT in the device error word and the kernel returns. */
 pop_status pop_set_wait_limit(pop_ffn_t h, uint64_t ns);
 
+/* Per-kernel timing of decode steps (off by default): while enabled, each pop_decode_step records
+ * CUDA events on its stream around its four kernels (gate/up over R u C, candidate selection,
+ * gathered down projection, reduction of partial sums), for up to 4096 steps between reads.
+ * Enabling creates the events; disabling destroys them. */
+pop_status pop_profile_enable(pop_ffn_t h, int enable);
+
+/* Sums of the recorded kernel durations in milliseconds since the last read: ms[0] gate/up,
+ * ms[1] selection, ms[2] down projection, ms[3] reduction; *steps receives the number of decode
+ * steps recorded. Clears the record. Syncs. */
+pop_status pop_profile_read(pop_ffn_t h, double* ms, int* steps);
+
 /* Synchronizes the device and returns the first recorded device-side failure (TIMEOUT or
  * DEVICE) or POP_OK; clears the error word. CUDA if a CUDA call fails. */
 pop_status pop_check(pop_ffn_t h);

@@ -60,6 +60,8 @@ SIGNATURES = {
     "pop_get_scores": (_i32, [_vp, _fp, _fp]),
     "pop_get_step": (_i32, [_vp, _ip]),
     "pop_set_wait_limit": (_i32, [_vp, _u64]),
+    "pop_profile_enable": (_i32, [_vp, _i32]),
+    "pop_profile_read": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _ip]),
     "pop_check": (_i32, [_vp]),
     "pop_last_error": (ctypes.c_char_p, [_vp]),
     "pop_status_string": (ctypes.c_char_p, [_i32]),
@@ -211,6 +213,18 @@ def pop_set_wait_limit(h, ns: int) -> None:
     _check(load_library().pop_set_wait_limit(h, ns), h)
 
 
+def pop_profile_enable(h, enable: bool = True) -> None:
+    _check(load_library().pop_profile_enable(h, 1 if enable else 0), h)
+
+
+def pop_profile_read(h):
+    """(ms per kernel [gate/up, select, down, reduce] summed since the last read, decode steps)."""
+    ms = (ctypes.c_double * 4)()
+    steps = ctypes.c_int()
+    _check(load_library().pop_profile_read(h, ms, ctypes.byref(steps)), h)
+    return list(ms), steps.value
+
+
 def pop_check(h) -> None:
     _check(load_library().pop_check(h), h)
 
@@ -288,6 +302,12 @@ class PopFFN:
 
     def set_wait_limit(self, ns: int):
         pop_set_wait_limit(self.handle, ns)
+
+    def profile(self, enable: bool = True):
+        pop_profile_enable(self.handle, enable)
+
+    def profile_read(self):
+        return pop_profile_read(self.handle)
 
     def check(self):
         pop_check(self.handle)

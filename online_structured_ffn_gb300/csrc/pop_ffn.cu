@@ -44,8 +44,14 @@ struct pop_ffn {
   bool partitioned = false;
   bool selected = false;
   uint64_t wait_ns = 2000000000ull;
+  // optional per-kernel timing of decode steps: kProfEvents events per step
+  std::vector<cudaEvent_t> prof_events;
+  int prof_steps = 0;
   std::string msg;
 };
+
+static constexpr int kProfEvents = 5;
+static constexpr int kProfMaxSteps = 4096;
 
 namespace {
 thread_local std::string g_msg;
@@ -79,6 +85,18 @@ cudaError_t dalloc(T** p, size_t count) {
 }
 
 PackedWeights packed(const pop_ffn* h) { return PackedWeights{h->Wp, h->n2, h->D, h->N}; }
+
+void destroy_events(pop_ffn* h) {
+  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+  h->prof_events.clear();
+  h->prof_steps = 0;
+}
+
+// Records profiling event `i` of the current decode step when timing is on and there is room.
+void prof_mark(pop_ffn* h, int i, cudaStream_t st) {
+  if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps)
+    cudaEventRecord(h->prof_events[static_cast<size_t>(h->prof_steps) * kProfEvents + i], st);
+}
 
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp, h->n2, h->Z, h->part, h->sumsq, h->I, h->rc, h->P, h->idx_all,
@@ -224,6 +242,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
 void pop_ffn_destroy(pop_ffn_t h) {
   if (!h) return;
   cudaDeviceSynchronize();
+  destroy_events(h);
   free_all(h);
   delete h;
 }
@@ -329,13 +348,19 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const PackedWeights w = packed(h);
   const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
+  prof_mark(h, 0, st);
   POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
                                    h->err, h->num_sms, st));
+  prof_mark(h, 1, st);
   POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+  prof_mark(h, 2, st);
   int G = 0;
   POP_CUDA(h, launch_down_decode(w, h->rc, nC, nR, h->S, h->cnt.k, h->z, nRC, B, h->ypart,
                                  h->ypart_parts / (B == 1 ? 1 : B), &G, h->err, h->num_sms, st));
+  prof_mark(h, 3, st);
   POP_CUDA(h, launch_reduce_y(h->ypart, G, B, h->D, y, h->cfg.out_f32, st));
+  prof_mark(h, 4, st);
+  if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps) ++h->prof_steps;
   h->selected = true;
   return POP_OK;
 }
@@ -405,6 +430,42 @@ pop_status pop_get_step(pop_ffn_t h, int* step) {
   if (!h || !step) return fail(h, POP_ERR_INVALID_ARG, "pop_get_step: NULL argument");
   POP_CUDA(h, cudaDeviceSynchronize());
   POP_CUDA(h, cudaMemcpy(step, h->step, sizeof(int), cudaMemcpyDeviceToHost));
+  return POP_OK;
+}
+
+pop_status pop_profile_enable(pop_ffn_t h, int enable) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_profile_enable: NULL handle");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  destroy_events(h);
+  if (!enable) return POP_OK;
+  h->prof_events.resize(static_cast<size_t>(kProfEvents) * kProfMaxSteps);
+  for (auto& e : h->prof_events) {
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) {
+      e = nullptr;
+      h->prof_events.erase(std::remove(h->prof_events.begin(), h->prof_events.end(), nullptr), h->prof_events.end());
+      destroy_events(h);
+      return cuda_fail(h, r, "cudaEventCreate");
+    }
+  }
+  return POP_OK;
+}
+
+pop_status pop_profile_read(pop_ffn_t h, double* ms, int* steps) {
+  if (!h || !ms || !steps) return fail(h, POP_ERR_INVALID_ARG, "pop_profile_read: NULL argument");
+  for (int i = 0; i < kProfEvents - 1; ++i) ms[i] = 0.0;
+  *steps = h->prof_steps;
+  if (h->prof_events.empty()) return fail(h, POP_ERR_STATE, "pop_profile_read: profiling is not enabled");
+  POP_CUDA(h, cudaDeviceSynchronize());
+  for (int s = 0; s < h->prof_steps; ++s) {
+    for (int i = 0; i < kProfEvents - 1; ++i) {
+      float t = 0.f;
+      POP_CUDA(h, cudaEventElapsedTime(&t, h->prof_events[static_cast<size_t>(s) * kProfEvents + i],
+                                       h->prof_events[static_cast<size_t>(s) * kProfEvents + i + 1]));
+      ms[i] += t;
+    }
+  }
+  h->prof_steps = 0;
   return POP_OK;
 }
 
