@@ -65,6 +65,7 @@ typedef enum {
 #define POP_MAX_D 16384        /* D must be a multiple of 8 and <= POP_MAX_D */
 #define POP_MAX_D_FF 49152     /* D_FF <= POP_MAX_D_FF (the partition runs in one CTA) */
 #define POP_MAX_BATCH 64       /* max_batch <= POP_MAX_BATCH */
+#define POP_STATIC_MAX_D_FF 49152  /* largest D_FF of pop_ffn_dense_token_noalloc (its static scratch) */
 
 typedef struct {
   int D;                  /* model width: length of x and y. Multiple of 8, 8..POP_MAX_D. */
@@ -173,6 +174,26 @@ pop_status pop_check(pop_ffn_t h);
 /* Message of the last failed call on h (h == NULL: last failure of pop_ffn_create or of a call
  * given a NULL handle). Valid until the next call on the same handle. Never NULL. */
 const char* pop_last_error(pop_ffn_t h);
+
+/* Dense FFN of one token without any device allocation, for callers that cannot allocate GPU
+ * memory when they run: processes whose device memory is reserved up front by their own memory
+ * manager, and latency-critical loops that must not enter the CUDA allocator (it can block and
+ * synchronise the device). The POP notes and the other pages have no counterpart to this call;
+ * it is a deployment convenience of this library.
+ *   Wg, W1: device bf16 [D_FF, D]; W2: device bf16 [D, D_FF] (row-major, as for pop_ffn_create);
+ *   x: device bf16 [D]; y: device [D], float32 if out_f32 else bf16. No handle is involved.
+ *   D: multiple of 8 in [8, POP_MAX_D]; D_FF: multiple of 8, at most POP_STATIC_MAX_D_FF.
+ * Computes y = W2 (SiLU(Wg x) (.) W1 x), asynchronously on `stream`. The intermediate z lives in
+ * one static device array of POP_STATIC_MAX_D_FF floats (192 KB), held by every GPU that loads
+ * the library until the process exits. All calls on a device share it and it keeps the last
+ * call's contents; every call rewrites all of z before reading it, but calls that overlap on the
+ * GPU (other streams, other host threads) race on it and must be serialised by the caller.
+ * The first call on each device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Errors: INVALID_ARG (NULL or misaligned pointer, D or D_FF outside the limits above, with the
+ * message in pop_last_error(NULL)), UNSUPPORTED (not sm_103), CUDA. Calls no cudaMalloc/cudaFree. */
+pop_status pop_ffn_dense_token_noalloc(const void* Wg, const void* W1, const void* W2, int D, int D_FF,
+                                       const void* x, void* y, int out_f32, void* stream);
 
 /* Name of a status code. Never NULL. */
 const char* pop_status_string(pop_status s);

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libpopffn.so")
 
 POP_OK, POP_ERR_INVALID_ARG, POP_ERR_STATE, POP_ERR_CUDA, POP_ERR_OOM, POP_ERR_TIMEOUT, POP_ERR_UNSUPPORTED, \
     POP_ERR_DEVICE = range(8)
-POP_MAX_D, POP_MAX_D_FF, POP_MAX_BATCH = 16384, 49152, 64
+POP_MAX_D, POP_MAX_D_FF, POP_MAX_BATCH, POP_STATIC_MAX_D_FF = 16384, 49152, 64, 49152
 
 
 class pop_config(ctypes.Structure):
@@ -62,6 +62,7 @@ SIGNATURES = {
     "pop_set_wait_limit": (_i32, [_vp, _u64]),
     "pop_profile_enable": (_i32, [_vp, _i32]),
     "pop_profile_read": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _ip]),
+    "pop_ffn_dense_token_noalloc": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
     "pop_check": (_i32, [_vp]),
     "pop_last_error": (ctypes.c_char_p, [_vp]),
     "pop_status_string": (ctypes.c_char_p, [_i32]),

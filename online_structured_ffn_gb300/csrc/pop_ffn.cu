@@ -111,6 +111,8 @@ __global__ void k_iota(int* a, int n) {
 }
 }  // namespace
 
+void pop::set_unbound_error(const char* msg) { g_msg = msg; }
+
 extern "C" {
 
 const char* pop_status_string(pop_status s) {

@@ -72,4 +72,7 @@ cudaError_t launch_prefill_down(const CUtensorMap& z_map, const PrefillMaps& map
                                 int out_f32, unsigned* err, uint64_t wait_ns, int num_sms, cudaStream_t st);
 size_t prefill_smem_bytes();
 
+// Sets the message that pop_last_error(NULL) returns on this thread.
+void set_unbound_error(const char* msg);
+
 }  // namespace pop
