@@ -167,6 +167,13 @@ pop_status pop_profile_enable(pop_ffn_t h, int enable);
  * steps recorded. Clears the record. Syncs. */
 pop_status pop_profile_read(pop_ffn_t h, double* ms, int* steps);
 
+/* Options of a handle. POP_OPT_FUSED_DECODE (default 1): run a B = 1 decode step as one persistent
+ * kernel (gate/up, top-k and down in a single cooperative launch) when |C| <= 8192 and the shared
+ * memory fits; 0 forces the four-kernel path (gate/up, selection, down, reduction). Both give
+ * the same selection; y differs only by summation order. */
+#define POP_OPT_FUSED_DECODE 1
+pop_status pop_set_option(pop_ffn_t h, int option, int value);
+
 /* Synchronizes the device and returns the first recorded device-side failure (TIMEOUT or
  * DEVICE) or POP_OK; clears the error word. CUDA if a CUDA call fails. */
 pop_status pop_check(pop_ffn_t h);

@@ -41,6 +41,9 @@ struct pop_ffn {
   int ypart_parts = 0;  // capacity in units of D floats
   int* step = nullptr;
   unsigned* err = nullptr;
+  unsigned* fsync = nullptr;  // inter-CTA counters of the fused decode step
+  int fused_stages = 0;       // 0: the fused step cannot run these sizes
+  bool fused_on = true;
   bool partitioned = false;
   bool selected = false;
   uint64_t wait_ns = 2000000000ull;
@@ -100,7 +103,7 @@ void prof_mark(pop_ffn* h, int i, cudaStream_t st) {
 
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp, h->n2, h->Z, h->part, h->sumsq, h->I, h->rc, h->P, h->idx_all,
-                  h->z,  h->scores, h->memory, h->S, h->ypart, h->step, h->err};
+                  h->z,  h->scores, h->memory, h->S, h->ypart, h->step, h->err, h->fsync};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -221,7 +224,10 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
   POP_ALLOC(h->step, 1);
   POP_ALLOC(h->err, 1);
+  POP_ALLOC(h->fsync, 4);
 #undef POP_ALLOC
+  if ((e = cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  h->fused_stages = decode_fused_stages(D, cnt.n_C);
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection
@@ -293,6 +299,7 @@ pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, voi
   if (s != POP_OK) return s;
   POP_CUDA(h, launch_partition(h->sumsq, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step,
                                h->memory, h->err, st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -305,6 +312,7 @@ pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, v
   POP_CUDA(h, cudaMemcpyAsync(h->I, importance, sizeof(float) * h->N, cudaMemcpyDeviceToDevice, st));
   POP_CUDA(h, launch_partition(nullptr, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step, h->memory,
                                h->err, st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -333,6 +341,7 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
   if (nP) POP_CUDA(h, cudaMemcpyAsync(h->P, P, sizeof(int) * nP, cudaMemcpyHostToDevice, st));
   POP_CUDA(h, cudaMemsetAsync(h->step, 0, sizeof(int), st));
   POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
   POP_CUDA(h, cudaStreamSynchronize(st));
   h->partitioned = true;
   h->selected = false;
@@ -350,6 +359,39 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const PackedWeights w = packed(h);
   const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
+  if (B == 1 && h->fused_on && h->fused_stages > 0 && h->num_sms <= h->ypart_parts) {
+    FusedDecodeArgs a{};
+    a.Wp = h->Wp;
+    a.n2 = h->n2;
+    a.D = h->D;
+    a.N = h->N;
+    a.x = static_cast<const uint16_t*>(x);
+    a.rc = h->rc;
+    a.nC = nC;
+    a.nR = nR;
+    a.k = h->cnt.k;
+    a.period = h->cfg.period;
+    a.zC = h->z;
+    a.scores = h->scores;
+    a.memory = h->memory;
+    a.S = h->S;
+    a.step = h->step;
+    a.ypart = h->ypart;
+    a.y = y;
+    a.out_f32 = h->cfg.out_f32;
+    a.sync = h->fsync;
+    a.err = h->err;
+    a.wait_ns = h->wait_ns;
+    a.stages = h->fused_stages;
+    // CTA 0 runs the top-k (a few microseconds) and gives up about 180 KB of R rows for it
+    a.r_skew = static_cast<int>((180 * 1024 + 6 * h->D - 1) / (6 * h->D));
+    prof_mark(h, 0, st);
+    POP_CUDA(h, launch_decode_fused_b1(a, h->num_sms, st));
+    for (int i = 1; i < kProfEvents; ++i) prof_mark(h, i, st);
+    if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps) ++h->prof_steps;
+    h->selected = true;
+    return POP_OK;
+  }
   prof_mark(h, 0, st);
   POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
                                    h->err, h->num_sms, st));
@@ -435,6 +477,15 @@ pop_status pop_get_step(pop_ffn_t h, int* step) {
   return POP_OK;
 }
 
+pop_status pop_set_option(pop_ffn_t h, int option, int value) {
+  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_set_option: NULL handle");
+  if (option == POP_OPT_FUSED_DECODE) {
+    h->fused_on = value != 0;
+    return POP_OK;
+  }
+  return fail(h, POP_ERR_INVALID_ARG, "pop_set_option: unknown option");
+}
+
 pop_status pop_profile_enable(pop_ffn_t h, int enable) {
   if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_profile_enable: NULL handle");
   POP_CUDA(h, cudaDeviceSynchronize());
@@ -480,7 +531,8 @@ pop_status pop_check(pop_ffn_t h) {
   POP_CUDA(h, cudaMemset(h->err, 0, sizeof(unsigned)));
   char buf[200];
   std::snprintf(buf, sizeof buf,
-                "device error word 0x%x (1/2: gate-up/down wait ran out; 4: partition; 8: top-k; 16: index)", e);
+                "device error word 0x%x (1/2/32: prefill gate-up / prefill down / fused decode wait ran out; "
+                "4: partition; 8: top-k; 16: index)", e);
   return fail(h, (e & DEVERR_TIMEOUT_ANY) ? POP_ERR_TIMEOUT : POP_ERR_DEVICE, buf);
 }
 

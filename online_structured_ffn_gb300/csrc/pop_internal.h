@@ -13,7 +13,8 @@ enum : unsigned {
   DEVERR_PARTITION = 1u << 2,       // partition: region sizes did not match the counts
   DEVERR_TOPK = 1u << 3,            // top-k: selected count did not match k
   DEVERR_INDEX = 1u << 4,           // an index list entry was out of range
-  DEVERR_TIMEOUT_ANY = DEVERR_TIMEOUT_GATEUP | DEVERR_TIMEOUT_DOWN,
+  DEVERR_TIMEOUT_DECODE = 1u << 5,  // fused decode step: a wait ran out
+  DEVERR_TIMEOUT_ANY = DEVERR_TIMEOUT_GATEUP | DEVERR_TIMEOUT_DOWN | DEVERR_TIMEOUT_DECODE,
 };
 
 // Packed weights: row i of Wp holds [Wg[i, 0:D] | W1[i, 0:D] | W2[0:D, i]] (3*D bf16).
@@ -40,6 +41,35 @@ cudaError_t launch_down_decode(const PackedWeights& w, const int* rc, int nC, in
 int down_decode_parts(int D, int B, int nitems, int num_sms);
 // y[b][d] = sum_g ypart[g][b][d] (g ascending); y is fp32 or bf16.
 cudaError_t launch_reduce_y(const float* ypart, int G, int B, int D, void* y, int out_f32, cudaStream_t st);
+
+// ---- fused decode step for B = 1 (pop_fused.cu)
+constexpr int FZ_MAX_C = 8192;  // largest |C| the fused step handles (its top-k keys sit in shared memory)
+struct FusedDecodeArgs {
+  const uint16_t* Wp;
+  const float* n2;
+  int D, N;
+  const uint16_t* x;  // [D] bf16
+  const int* rc;      // [C | R] channel indices
+  int nC, nR, k, period;
+  float* zC;          // [nC] z of the candidates
+  float* scores;      // [nC]
+  float* memory;      // [nC]
+  int* S;             // [k] selected positions into C
+  int* step;
+  float* ypart;       // [grid][D] partial sums
+  void* y;
+  int out_f32;
+  unsigned* sync;     // 4 counters, all 0 before the first launch: C arrivals, selection generation,
+                      // grid-barrier arrivals, grid-barrier generation
+  unsigned* err;
+  uint64_t wait_ns;
+  int stages;         // ring stages of 6*D bytes
+  int r_skew;         // R channels CTA 0 gives up to make room for the top-k
+};
+// Stages that fit for (D, |C|), or 0 when the fused step cannot run those sizes.
+int decode_fused_stages(int D, int nC);
+size_t decode_fused_smem(int D, int nC, int stages);
+cudaError_t launch_decode_fused_b1(const FusedDecodeArgs& a, int num_sms, cudaStream_t st);
 
 // ---- selection (pop_select.cu)
 // Importance from channel sums (if sumsq != NULL: I = n2 * sqrt(sumsq), written to I), then the

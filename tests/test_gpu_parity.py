@@ -146,7 +146,7 @@ def test_decode_parity(env, B):
     lay.close()
 
 
-@pytest.mark.parametrize("D,N", [(264, 1000), (1024, 4096), (4096, 1100)])
+@pytest.mark.parametrize("D,N", [(264, 1000), (1024, 4096), (4096, 1100), (16384, 512)])
 def test_decode_parity_shapes(env, D, N):
     lay = Layer(env, D, N, r=0.299, gamma=0.1, max_batch=16)
     Wg, W1, W2 = lay.w64()
@@ -154,6 +154,56 @@ def test_decode_parity_shapes(env, D, N):
     for B in (1, 16):
         _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), B, steps=3)
     lay.close()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("D,N,r,gamma,period", [(512, 2048, 0.3, 0.1, 1), (4096, 11008, 0.299, 0.1, 1),
+                                                (256, 1024, 0.5, 0.1, 4), (1024, 600, 0.3, 0.0, 1),
+                                                (1024, 600, 0.4, 0.6, 1), (2048, 333, 0.0, 0.1, 1)])
+def test_single_token_paths(env, fused, D, N, r, gamma, period):
+    # B = 1 runs as one persistent kernel by default; the four-kernel path is the other option.
+    lay = Layer(env, D, N, r=r, gamma=gamma, period=period)
+    lay.ffn.set_fused_decode(fused)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 8, lay.sc)), r, gamma)
+    if period == 1:
+        _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), 1, steps=4)
+    else:
+        lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+        sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k, period=period)
+        for t in range(2 * period + 1):
+            x = synth.decode_input(0, t, 1, lay.sc)
+            mem_before = sess.memory.copy()
+            y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+            y_ref = sess.step(f64(x))
+            if t % period == 0:
+                bad, _, nd = parity.compare_selection(lay.ffn.selected(), sess.C[sess.S], sess.C,
+                                                      mem_before + sess.last_scores, lay.counts.k)
+                assert not bad
+                if nd:
+                    continue
+            parity.check_y(y, y_ref, f"step {t}")
+        lay.ffn.check()
+    lay.close()
+
+
+def test_fused_step_is_repeatable(env):
+    # the persistent kernel reduces its partial sums in a fixed order: identical runs, identical y
+    _, torch, dev = env
+    D, N = 1024, 4096
+    a = Layer(env, D, N, r=0.3, gamma=0.1)
+    b = Layer(env, D, N, r=0.3, gamma=0.1)
+    X = up(env, synth.prompt(0, 64, a.sc))
+    a.ffn.prefill_partition(X)
+    b.ffn.prefill_partition(X)
+    for t in range(5):
+        x = up(env, synth.decode_input(0, t, 1, a.sc))
+        ya, yb = a.ffn.decode_step(x), b.ffn.decode_step(x)
+        assert torch.equal(ya, yb)
+        assert np.array_equal(a.ffn.selected(), b.ffn.selected())
+    a.ffn.check()
+    a.close()
+    b.close()
 
 
 @pytest.mark.parametrize("period,B", [(4, 1), (4, 4), (16, 2)])
