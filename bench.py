@@ -46,6 +46,8 @@ WORKLOADS = {
                                   layers=1, chunk=8192),
 }
 METRIC = "pruned-FFN decode tokens/s and HBM GB/s vs GB300 peak, LLaMA-7B FFN, B=1/16"
+# one decode step in PROFILE_STRIDE records CUDA events around its kernels (events cost GPU time)
+PROFILE_STRIDE = 8
 UNIT = "tokens/s"
 
 
@@ -194,11 +196,13 @@ class Stack:
         self.counts = self.ffn[0].counts
         self.chunks = (M + wl["chunk"] - 1) // wl["chunk"]
 
-    def launches_per_session(self, fused: bool):
+    def launches_per_session(self):
         # prefill: per chunk gate/up GEMM + sum fold + down GEMM, then the partition kernel;
-        # decode: one persistent kernel per layer and step (B = 1), else gate/up, selection, down,
-        # reduction
-        per_layer = 3 * self.chunks + 1 + (1 if fused else 4) * self.wl["T"]
+        # decode at B = 1: gate/up with the top-k inside (+ a separate top-k when |C| > 8192) and the
+        # tiled down projection; at B > 1: gate/up, selection, down, reduction
+        c = self.counts
+        per_step = (2 + (1 if c.n_C > 8192 else 0)) if self.wl["B"] == 1 else 4
+        per_layer = 3 * self.chunks + 1 + per_step * self.wl["T"]
         return per_layer * self.wl["layers"]
 
     def session(self, dec_events=None):
@@ -259,7 +263,7 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
         stack.session()
     torch.cuda.synchronize()
     for f in stack.ffn:
-        f.profile(True)
+        f.profile(PROFILE_STRIDE)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(torch.cuda.current_device()) if with_clocks else None
@@ -289,24 +293,21 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     c = stack.counts
     gu_bytes, dn_bytes = touched_bytes(c, wl["D"])
     peak, peak_kind = measured_peaks()
-    # one persistent kernel per step (the library records no time for the other three slots)
-    fused = sum(ksum[1:]) < 1e-3 * ksum[0]
     gu_ms = ksum[0] / max(nsteps, 1)
-    roof_bytes = gu_bytes + dn_bytes if fused else gu_bytes
+    roof_bytes = gu_bytes
     dec_step_s = dec_s / (T * Lyr * steps)
     res = dict(
         value=g_units / g_elapsed, elapsed=g_elapsed, units=g_units, ms_per_step=1e3 * g_elapsed / steps,
         decode_only_tokens_per_s=B * T * Lyr * steps / dec_s,
         decode_step_us=1e6 * dec_step_s,
         prefill_ms_per_layer=1e3 * (elapsed - dec_s) / (steps * Lyr),
-        kernel_us=({"fused_step": 1e3 * ksum[0] / max(nsteps, 1)} if fused else
-                   {n: 1e3 * ksum[i] / max(nsteps, 1) for i, n in enumerate(("gateup", "select", "down", "reduce"))}),
-        fused=fused, roof_bytes=roof_bytes,
+        kernel_us={n: 1e3 * ksum[i] / max(nsteps, 1) for i, n in enumerate(("gateup", "select", "down", "reduce"))},
+        roof_bytes=roof_bytes,
         gateup_gbs=roof_bytes / (gu_ms * 1e-3) / 1e9,
         peak=peak, peak_kind=peak_kind,
         step_gbs=(gu_bytes + dn_bytes) / dec_step_s / 1e9,
         gu_bytes=gu_bytes, dn_bytes=dn_bytes, counts=c.as_dict(),
-        launches=stack.launches_per_session(fused) * steps,
+        launches=stack.launches_per_session() * steps,
         clocks=sampler.summary() if sampler else None,
     )
     if with_e2e:
@@ -400,7 +401,7 @@ def traffic_from_profiles(kernel: str, workload: str):
         text = open(path).read()
     except OSError:
         return None
-    src_name = "pop_fused.cu" if kernel == "fused_decode" else "pop_decode.cu"
+    src_name = "pop_decode1.cu" if workload.endswith("-b1") else "pop_decode.cu"
     src = open(os.path.join(ROOT, "online_structured_ffn_gb300", "csrc", src_name), "rb").read()
     sha = hashlib.sha256(src).hexdigest()[:16]
     vals = {}
@@ -476,22 +477,21 @@ def main():
                      "decode_only_tokens_per_s": s["decode_only_tokens_per_s"],
                      "decode_step_us": s["decode_step_us"], "kernel_us": s["kernel_us"],
                      "gateup_hbm_gbs": s["gateup_gbs"], "gateup_frac": s["gateup_gbs"] / s["peak"],
-                     "fused": s["fused"],
                      "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"]}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
     if rank != 0:
         return
-    traffic = traffic_from_profiles("fused_decode" if res["fused"] else "gateup_decode", args.workload)
+    traffic = traffic_from_profiles("gateup_decode", args.workload)
     line = {
         "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator)",
         "config": config,
         "roofline": {"bound": "hbm",
-                     "kernel": ("k_decode_fused_b1 (whole decode step: gate/up over R u C, top-k, down over R u S)"
-                                if res["fused"] else "k_gateup_b1 (decode gate/up over R u C)"),
+                     "kernel": ("k_gateup_sel_b1 (decode gate/up over R u C, top-k inside)" if wl["B"] == 1
+                                else "k_gateup_mma (decode gate/up over R u C, B > 1)"),
                      "achieved": res["gateup_gbs"], "peak": res["peak"], "unit": "GB/s",
                      "frac": res["gateup_gbs"] / res["peak"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": res["roof_bytes"], "peak_source": res["peak_kind"]},

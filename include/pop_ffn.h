@@ -36,7 +36,8 @@
  *     are found on the host before anything is enqueued. pop_last_error() gives the message.
  *   - Device-side failures (a bounded wait that ran out, an index out of range) are recorded
  *     in a device error word and returned by pop_check().
- *   - A handle may be used from one host thread at a time.
+ *   - A handle may be used from one host thread at a time, and its calls must not overlap on the
+ *     GPU (use one stream per handle, or order the streams).
  */
 #ifndef POP_FFN_H
 #define POP_FFN_H
@@ -126,7 +127,10 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
  * x: device bf16 [B, D], 1 <= B <= max_batch; y: device [B, D] (float32 if out_f32 else bf16).
  * Computes z over R u C, candidate scores a_i = max_b |z_{b,i}| * ||W2[:,i]||, updates the memory,
  * selects the k best candidates when step % period == 0 (ties to the lower index), and writes
- * y = sum over R u S of z_i * W2[:,i]. No allocation and no host synchronization.
+ * y = sum over R u S of z_i * W2[:,i]. No allocation and no host synchronization. At B = 1 the
+ * step is two kernels launched with programmatic dependent launch (the next kernel's weight
+ * prefetch overlaps the previous kernel's tail); each waits for its predecessor before it touches
+ * data a previous call may still use.
  * STATE if no partition has been set. */
 pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* stream);
 
@@ -156,23 +160,17 @@ pop_status pop_get_step(pop_ffn_t h, int* step);
  * A wait that runs out sets POP_ERR_TIMEOUT in the device error word and the kernel returns. */
 pop_status pop_set_wait_limit(pop_ffn_t h, uint64_t ns);
 
-/* Per-kernel timing of decode steps (off by default): while enabled, each pop_decode_step records
- * CUDA events on its stream around its four kernels (gate/up over R u C, candidate selection,
- * gathered down projection, reduction of partial sums), for up to 4096 steps between reads.
- * Enabling creates the events; disabling destroys them. */
+/* Per-kernel timing of decode steps (off by default). enable = n >= 1: one pop_decode_step in
+ * every n records CUDA events on its stream between its kernel slots (gate/up, selection, down,
+ * reduction; a slot a path does not launch reads near zero), for up to 4096 timed steps between
+ * reads. Each event adds a little GPU time, which sampling keeps out of most steps.
+ * enable = 0 turns timing off. Enabling creates the events; disabling destroys them. */
 pop_status pop_profile_enable(pop_ffn_t h, int enable);
 
 /* Sums of the recorded kernel durations in milliseconds since the last read: ms[0] gate/up,
  * ms[1] selection, ms[2] down projection, ms[3] reduction; *steps receives the number of decode
  * steps recorded. Clears the record. Syncs. */
 pop_status pop_profile_read(pop_ffn_t h, double* ms, int* steps);
-
-/* Options of a handle. POP_OPT_FUSED_DECODE (default 1): run a B = 1 decode step as one persistent
- * kernel (gate/up, top-k and down in a single cooperative launch) when |C| <= 8192 and the shared
- * memory fits; 0 forces the four-kernel path (gate/up, selection, down, reduction). Both give
- * the same selection; y differs only by summation order. */
-#define POP_OPT_FUSED_DECODE 1
-pop_status pop_set_option(pop_ffn_t h, int option, int value);
 
 /* Synchronizes the device and returns the first recorded device-side failure (TIMEOUT or
  * DEVICE) or POP_OK; clears the error word. CUDA if a CUDA call fails. */

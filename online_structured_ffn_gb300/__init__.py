@@ -20,7 +20,6 @@ LIB_PATH = os.path.join(_PKG, "libpopffn.so")
 POP_OK, POP_ERR_INVALID_ARG, POP_ERR_STATE, POP_ERR_CUDA, POP_ERR_OOM, POP_ERR_TIMEOUT, POP_ERR_UNSUPPORTED, \
     POP_ERR_DEVICE = range(8)
 POP_MAX_D, POP_MAX_D_FF, POP_MAX_BATCH, POP_STATIC_MAX_D_FF = 16384, 49152, 64, 49152
-POP_OPT_FUSED_DECODE = 1
 
 
 class pop_config(ctypes.Structure):
@@ -61,7 +60,6 @@ SIGNATURES = {
     "pop_get_scores": (_i32, [_vp, _fp, _fp]),
     "pop_get_step": (_i32, [_vp, _ip]),
     "pop_set_wait_limit": (_i32, [_vp, _u64]),
-    "pop_set_option": (_i32, [_vp, _i32, _i32]),
     "pop_profile_enable": (_i32, [_vp, _i32]),
     "pop_profile_read": (_i32, [_vp, ctypes.POINTER(ctypes.c_double), _ip]),
     "pop_ffn_dense_token_noalloc": (_i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp]),
@@ -216,10 +214,6 @@ def pop_set_wait_limit(h, ns: int) -> None:
     _check(load_library().pop_set_wait_limit(h, ns), h)
 
 
-def pop_set_option(h, option: int, value: int) -> None:
-    _check(load_library().pop_set_option(h, option, value), h)
-
-
 def pop_profile_enable(h, enable: bool = True) -> None:
     _check(load_library().pop_profile_enable(h, 1 if enable else 0), h)
 
@@ -309,9 +303,6 @@ class PopFFN:
 
     def set_wait_limit(self, ns: int):
         pop_set_wait_limit(self.handle, ns)
-
-    def set_fused_decode(self, on: bool):
-        pop_set_option(self.handle, POP_OPT_FUSED_DECODE, 1 if on else 0)
 
     def profile(self, enable: bool = True):
         pop_profile_enable(self.handle, enable)

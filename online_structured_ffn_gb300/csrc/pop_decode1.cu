@@ -1,0 +1,362 @@
+// Decode step of the POP FFN for one token (B = 1): two launches, no waits between CTAs.
+//
+// ("POP: Online Structural Pruning..." notes, Key design 2: H_t = f(X_t; R u C), score only C,
+// fill |R| + k survivors; "Batch-wise adaptive pruning", abstract: periodic top-k with an
+// activation memory.)
+//
+// Launch 1, k_gateup_sel_b1: gate/up over R u C, one warp per channel streaming the channel's two
+// contiguous rows with 16-byte loads. Every worker warp scores its share of the candidates before
+// it streams its share of R, so all candidate scores exist a few microseconds into the kernel.
+// CTA 0 streams nothing: it waits (bounded) until the candidate count is complete, then runs the
+// periodic memory update and the top-k while the workers are still streaming R, so the selection
+// costs no time on the critical path. Progress is guaranteed: the workers wait on nobody, so CTA 0
+// never holds up a CTA it waits for, even when the grid does not fit on the GPU at once.
+//
+// Launch 2, k_down_tiled_b1: y = sum over R u S of z_i W2[:, i]. CTA (t, c) owns the 512-wide
+// tile t of y and the c-th chunk of the kept channels; 8 groups of 64 threads each read one
+// channel's 1 KB slice of the contiguous down column with 16-byte loads. The last chunk CTA to
+// finish a tile (atomic counter) adds the chunks' partial tiles in chunk order: no extra launch,
+// and the result does not depend on timing.
+//
+// Both kernels are launched with programmatic dependent launch when the caller's stream allows it:
+// before waiting for the previous kernel (griddepcontrol.wait) they only prefetch weight rows into
+// L2 (constant data); they read x, z and S and write z, S, y only after the wait, so the overlap
+// with the previous kernel's tail never races on data.
+#include "pop_device.cuh"
+#include "pop_internal.h"
+#include "pop_radix.cuh"
+
+namespace pop {
+
+namespace {
+constexpr int GS_THREADS = 256;
+constexpr int GS_WARPS = GS_THREADS / 32;
+constexpr int DT_THREADS = 512;
+constexpr int DT_TILE = 512;   // outputs per tile: 64 threads x 8
+constexpr int DT_GROUPS = DT_THREADS / (DT_TILE / 8);
+constexpr int DT_BATCH = 512;  // kept channels staged in shared memory at a time
+constexpr int DT_UNROLL = 8;
+
+struct BlockSync256 {
+  __device__ void operator()() const { __syncthreads(); }
+};
+
+__device__ __forceinline__ int guard_idx(int v, int n, unsigned* err) {
+  if (static_cast<unsigned>(v) >= static_cast<unsigned>(n)) {
+    atomicOr(err, DEVERR_INDEX);
+    return 0;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float silu_1(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+}  // namespace
+
+template <int NCHL>
+__global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_constant__ DecodeB1Args a) {
+  extern __shared__ float xs[];  // D floats of x (workers) or nC keys (selector)
+  __shared__ RadixScratch<GS_THREADS> sc;
+  __shared__ int s_ok;
+  const int D = a.D;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (cta == 0) {
+    // ---------------------------------------------------------------- selector
+    pdl_trigger();  // the next kernel may take free SM slots; it waits for this grid before using S
+    pdl_wait();     // S, memory and step may still be read by the previous step's kernels
+    if (a.do_select) {
+      if (threadIdx.x == 0) {
+        bool ok = true;
+        if (a.nC > 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_u32(a.sync) < static_cast<unsigned>(a.nC)) {
+            __nanosleep(200);
+            if (globaltimer_ns() - t0 > a.wait_ns) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (ok) atomicExch(a.sync, 0u);  // every candidate has been counted: ready for the next step
+        else atomicOr(a.err, DEVERR_TIMEOUT_DECODE);
+        __threadfence();
+        s_ok = ok;
+      }
+      __syncthreads();
+      if (s_ok) {
+        uint32_t* keys = reinterpret_cast<uint32_t*>(xs);
+        const int t = *a.step;
+        const bool sel = select_step<GS_THREADS>(
+            threadIdx.x, [&](int i) { return __ldcg(a.scores + i); }, a.memory, a.nC, a.k, a.period,
+            (t % a.period) == 0, keys, a.S, sc, BlockSync256());
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          if (!sel) atomicOr(a.err, DEVERR_TOPK);
+          *a.step = t + 1;
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ workers
+  const int W = G - 1, j = cta - 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cb0 = static_cast<int>(static_cast<long long>(j) * a.nC / W);
+  const int cb1 = static_cast<int>(static_cast<long long>(j + 1) * a.nC / W);
+  const int rb0 = a.nC + static_cast<int>(static_cast<long long>(j) * a.nR / W);
+  const int rb1 = a.nC + static_cast<int>(static_cast<long long>(j + 1) * a.nR / W);
+  const int c0 = cb0 + warp * (cb1 - cb0) / GS_WARPS, c1 = cb0 + (warp + 1) * (cb1 - cb0) / GS_WARPS;
+  const int r0 = rb0 + warp * (rb1 - rb0) / GS_WARPS, r1 = rb0 + (warp + 1) * (rb1 - rb0) / GS_WARPS;
+  const int nch = D >> 3;
+  const size_t row3 = 3 * static_cast<size_t>(D);
+  // constant data only before the wait: warm L2 with this warp's first channel
+  {
+    const int p = c0 < c1 ? c0 : (r0 < r1 ? r0 : -1);
+    if (p >= 0) {
+      const int ch = a.rc[p];
+      if (static_cast<unsigned>(ch) < static_cast<unsigned>(a.N)) {
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(a.Wp + static_cast<size_t>(ch) * row3);
+        for (int off = lane * 128; off < 4 * D; off += 32 * 128) prefetch_l2(row + off);
+      }
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
+  for (int c = threadIdx.x; c < nch; c += GS_THREADS) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + 8 * c);
+    reinterpret_cast<float4*>(xs + 8 * c)[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+    reinterpret_cast<float4*>(xs + 8 * c)[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+  }
+  __syncthreads();
+  constexpr int GRP = NCHL < 4 ? NCHL : 4;
+
+  auto item = [&](int p) {
+    const int ch = guard_idx(a.rc[p], a.N, a.err);
+    const uint16_t* rg = a.Wp + static_cast<size_t>(ch) * row3;
+    const uint16_t* ru = rg + D;
+    float ag0 = 0.f, ag1 = 0.f, au0 = 0.f, au1 = 0.f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < NCHL; j0 += GRP) {
+      uint4 vg[GRP], vu[GRP];
+#pragma unroll
+      for (int q = 0; q < GRP; ++q) {
+        const int c = lane + 32 * (j0 + q);
+        if (c < nch) {
+          vg[q] = ldg_stream(rg + 8 * c);
+          vu[q] = ldg_stream(ru + 8 * c);
+        } else {
+          vg[q] = make_uint4(0u, 0u, 0u, 0u);
+          vu[q] = vg[q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < GRP; ++q) {
+        const int c = lane + 32 * (j0 + q);
+        if (c < nch) {
+          const float4 xa = *reinterpret_cast<const float4*>(xs + 8 * c);
+          const float4 xb = *reinterpret_cast<const float4*>(xs + 8 * c + 4);
+          ag0 = fmaf(bf16lo(vg[q].x), xa.x, ag0);
+          ag1 = fmaf(bf16hi(vg[q].x), xa.y, ag1);
+          ag0 = fmaf(bf16lo(vg[q].y), xa.z, ag0);
+          ag1 = fmaf(bf16hi(vg[q].y), xa.w, ag1);
+          ag0 = fmaf(bf16lo(vg[q].z), xb.x, ag0);
+          ag1 = fmaf(bf16hi(vg[q].z), xb.y, ag1);
+          ag0 = fmaf(bf16lo(vg[q].w), xb.z, ag0);
+          ag1 = fmaf(bf16hi(vg[q].w), xb.w, ag1);
+          au0 = fmaf(bf16lo(vu[q].x), xa.x, au0);
+          au1 = fmaf(bf16hi(vu[q].x), xa.y, au1);
+          au0 = fmaf(bf16lo(vu[q].y), xa.z, au0);
+          au1 = fmaf(bf16hi(vu[q].y), xa.w, au1);
+          au0 = fmaf(bf16lo(vu[q].z), xb.x, au0);
+          au1 = fmaf(bf16hi(vu[q].z), xb.y, au1);
+          au0 = fmaf(bf16lo(vu[q].w), xb.z, au0);
+          au1 = fmaf(bf16hi(vu[q].w), xb.w, au1);
+        }
+      }
+    }
+    float ag = ag0 + ag1, au = au0 + au1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ag += __shfl_xor_sync(0xffffffffu, ag, o);
+      au += __shfl_xor_sync(0xffffffffu, au, o);
+    }
+    if (lane == 0) {
+      const float zz = silu_1(ag) * au;
+      a.z[p] = zz;
+      if (p < a.nC) a.scores[p] = fabsf(zz) * a.n2[ch];
+    }
+  };
+
+  for (int p = c0; p < c1; ++p) item(p);
+  if (a.do_select && c1 > c0 && lane == 0) {
+    __threadfence();
+    atomicAdd(a.sync, static_cast<unsigned>(c1 - c0));
+  }
+  for (int p = r0; p < r1; ++p) item(p);
+}
+
+__global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_constant__ DecodeB1Args a) {
+  __shared__ int s_ch[DT_BATCH];
+  __shared__ float s_z[DT_BATCH];
+  __shared__ __align__(16) float red[DT_GROUPS][DT_TILE];
+  __shared__ int s_last;
+  const int D = a.D;
+  const int tile = blockIdx.x, chunk = blockIdx.y, NCK = gridDim.y;
+  const int grp = threadIdx.x / (DT_TILE / 8), tt = threadIdx.x % (DT_TILE / 8);
+  const int d = tile * DT_TILE + 8 * tt;
+  const bool dok = d < D;
+  const long long n = static_cast<long long>(a.nR) + a.kd;
+  const int i0 = static_cast<int>(chunk * n / NCK), i1 = static_cast<int>((chunk + 1) * n / NCK);
+  const size_t row3 = 3 * static_cast<size_t>(D);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  // constant data only before the wait: warm L2 with this CTA's slices of the retained channels'
+  // down columns (one thread per 128-byte line)
+  if (dok && (tt & 7) == 0) {
+    const int rlim = min(i1, a.nR);
+    for (int it = i0 + grp; it < rlim; it += DT_GROUPS) {
+      const int ch = a.rc[a.nC + it];
+      if (static_cast<unsigned>(ch) < static_cast<unsigned>(a.N))
+        prefetch_l2(a.Wp + static_cast<size_t>(ch) * row3 + 2 * static_cast<size_t>(D) + d);
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
+
+  for (int base = i0; base < i1; base += DT_BATCH) {
+    const int cnt = min(DT_BATCH, i1 - base);
+    __syncthreads();
+    for (int e = threadIdx.x; e < cnt; e += DT_THREADS) {
+      const int it = base + e;
+      const int pos = it < a.nR ? a.nC + it : guard_idx(a.S[it - a.nR], a.nC, a.err);
+      s_ch[e] = guard_idx(a.rc[pos], a.N, a.err);
+      s_z[e] = a.z[pos];
+    }
+    __syncthreads();
+    for (int ii = grp; ii < cnt; ii += DT_GROUPS * DT_UNROLL) {
+      uint4 v[DT_UNROLL];
+      float zz[DT_UNROLL];
+#pragma unroll
+      for (int u = 0; u < DT_UNROLL; ++u) {
+        const int idx = ii + DT_GROUPS * u;
+        const bool ok = idx < cnt && dok;
+        v[u] = ok ? ldg_stream(a.Wp + static_cast<size_t>(s_ch[idx]) * row3 + 2 * static_cast<size_t>(D) + d)
+                  : make_uint4(0u, 0u, 0u, 0u);
+        zz[u] = idx < cnt ? s_z[idx] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < DT_UNROLL; ++u) {
+        acc[0] = fmaf(bf16lo(v[u].x), zz[u], acc[0]);
+        acc[1] = fmaf(bf16hi(v[u].x), zz[u], acc[1]);
+        acc[2] = fmaf(bf16lo(v[u].y), zz[u], acc[2]);
+        acc[3] = fmaf(bf16hi(v[u].y), zz[u], acc[3]);
+        acc[4] = fmaf(bf16lo(v[u].z), zz[u], acc[4]);
+        acc[5] = fmaf(bf16hi(v[u].z), zz[u], acc[5]);
+        acc[6] = fmaf(bf16lo(v[u].w), zz[u], acc[6]);
+        acc[7] = fmaf(bf16hi(v[u].w), zz[u], acc[7]);
+      }
+    }
+  }
+  reinterpret_cast<float4*>(&red[grp][8 * tt])[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  reinterpret_cast<float4*>(&red[grp][8 * tt])[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  const int e = tile * DT_TILE + threadIdx.x;
+  if (threadIdx.x < DT_TILE && e < D) {
+    float s = 0.f;
+#pragma unroll
+    for (int g = 0; g < DT_GROUPS; ++g) s += red[g][threadIdx.x];
+    a.ypart[static_cast<size_t>(chunk) * D + e] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.tile_cnt + tile, 1u) == static_cast<unsigned>(NCK) - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < DT_TILE && e < D) {
+    float t = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < NCK; ++c) t += __ldcg(a.ypart + static_cast<size_t>(c) * D + e);
+    if (a.out_f32)
+      static_cast<float*>(a.y)[e] = t;
+    else
+      static_cast<__nv_bfloat16*>(a.y)[e] = __float2bfloat16_rn(t);
+  }
+  if (threadIdx.x == 0) atomicExch(a.tile_cnt + tile, 0u);
+}
+
+// ------------------------------------------------------------------ launchers
+static int pow2_ceil(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <class K>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const DecodeB1Args& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st) {
+  const int nchl = pow2_ceil((a.D / 8 + 31) / 32);
+  const size_t keys = a.do_select ? static_cast<size_t>(a.nC > 0 ? a.nC : 1) * sizeof(uint32_t) : 0;
+  const size_t xsz = static_cast<size_t>(a.D) * sizeof(float);
+  const size_t smem = keys > xsz ? keys : xsz;
+#define POP_GS(NC)                                                                                              \
+  case NC: {                                                                                                    \
+    static size_t configured = 0;                                                                               \
+    if (smem > 48 * 1024 && smem > configured) {                                                                \
+      cudaError_t e = cudaFuncSetAttribute(k_gateup_sel_b1<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                           static_cast<int>(smem));                                             \
+      if (e != cudaSuccess) return e;                                                                           \
+      configured = smem;                                                                                        \
+    }                                                                                                           \
+    { cudaError_t e = launch_pdl(k_gateup_sel_b1<NC>, dim3(grid), dim3(GS_THREADS), smem, st, a);             \
+      if (e != cudaSuccess) return e; }                                                                         \
+    break;                                                                                                      \
+  }
+  switch (nchl) {
+    POP_GS(1) POP_GS(2) POP_GS(4) POP_GS(8) POP_GS(16) POP_GS(32) POP_GS(64)
+    default: return cudaErrorInvalidValue;
+  }
+#undef POP_GS
+  return cudaGetLastError();
+}
+
+int down_tiled_chunks(int D, int nitems, int num_sms) {
+  const int tiles = (D + DT_TILE - 1) / DT_TILE;
+  int nck = (2 * num_sms + tiles - 1) / tiles;
+  if (nck > nitems) nck = nitems;
+  return nck < 1 ? 1 : nck;
+}
+
+cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st) {
+  const int tiles = (a.D + DT_TILE - 1) / DT_TILE;
+  const int nck = down_tiled_chunks(a.D, a.nR + a.kd, num_sms);
+  return launch_pdl(k_down_tiled_b1, dim3(tiles, nck), dim3(DT_THREADS), 0, st, a);
+}
+
+}  // namespace pop

@@ -41,19 +41,22 @@ struct pop_ffn {
   int ypart_parts = 0;  // capacity in units of D floats
   int* step = nullptr;
   unsigned* err = nullptr;
-  unsigned* fsync = nullptr;  // inter-CTA counters of the fused decode step
-  int fused_stages = 0;       // 0: the fused step cannot run these sizes
-  bool fused_on = true;
+  unsigned* fsync = nullptr;  // inter-CTA counters of the decode kernels
   bool partitioned = false;
   bool selected = false;
   uint64_t wait_ns = 2000000000ull;
   // optional per-kernel timing of decode steps: kProfEvents events per step
   std::vector<cudaEvent_t> prof_events;
   int prof_steps = 0;
+  int prof_stride = 1;    // time one decode step in every prof_stride
+  long long prof_calls = 0;
+  bool prof_now = false;  // the current decode step is being timed
   std::string msg;
 };
 
 static constexpr int kProfEvents = 5;
+// device counters: [4] candidates scored by the B = 1 gate/up, [8..] tiles of y done by the down chunks
+static constexpr int kSyncWords = 64;
 static constexpr int kProfMaxSteps = 4096;
 
 namespace {
@@ -93,12 +96,22 @@ void destroy_events(pop_ffn* h) {
   for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
   h->prof_events.clear();
   h->prof_steps = 0;
+  h->prof_calls = 0;
 }
 
 // Records profiling event `i` of the current decode step when timing is on and there is room.
+void prof_begin(pop_ffn* h) {
+  h->prof_now = !h->prof_events.empty() && h->prof_steps < kProfMaxSteps && (h->prof_calls % h->prof_stride) == 0;
+  ++h->prof_calls;
+}
+
 void prof_mark(pop_ffn* h, int i, cudaStream_t st) {
-  if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps)
-    cudaEventRecord(h->prof_events[static_cast<size_t>(h->prof_steps) * kProfEvents + i], st);
+  if (h->prof_now) cudaEventRecord(h->prof_events[static_cast<size_t>(h->prof_steps) * kProfEvents + i], st);
+}
+
+void prof_end(pop_ffn* h) {
+  if (h->prof_now) ++h->prof_steps;
+  h->prof_now = false;
 }
 
 void free_all(pop_ffn* h) {
@@ -106,6 +119,32 @@ void free_all(pop_ffn* h) {
                   h->z,  h->scores, h->memory, h->S, h->ypart, h->step, h->err, h->fsync};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+}
+
+DecodeB1Args b1_args(pop_ffn* h, const uint16_t* x, void* y, const int* rc, int nC, int nR) {
+  DecodeB1Args a{};
+  a.Wp = h->Wp;
+  a.n2 = h->n2;
+  a.D = h->D;
+  a.N = h->N;
+  a.x = x;
+  a.rc = rc;
+  a.nC = nC;
+  a.nR = nR;
+  a.period = h->cfg.period;
+  a.z = h->z;
+  a.scores = h->scores;
+  a.memory = h->memory;
+  a.S = h->S;
+  a.step = h->step;
+  a.ypart = h->ypart;
+  a.y = y;
+  a.out_f32 = h->cfg.out_f32;
+  a.sync = h->fsync + 4;
+  a.tile_cnt = h->fsync + 8;
+  a.err = h->err;
+  a.wait_ns = h->wait_ns;
+  return a;
 }
 
 __global__ void k_iota(int* a, int n) {
@@ -195,7 +234,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   h->ldZ = round_up(N, 128);
   h->ldPart = h->ldZ;
   const int gk = down_decode_parts(D, 2, 1 << 30, h->num_sms);
-  h->ypart_parts = std::max(h->num_sms, gk * cfg->max_batch);
+  h->ypart_parts = std::max(2 * h->num_sms, gk * cfg->max_batch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   auto bail = [&](cudaError_t err, const char* where) {
@@ -224,10 +263,10 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
   POP_ALLOC(h->step, 1);
   POP_ALLOC(h->err, 1);
-  POP_ALLOC(h->fsync, 4);
+  POP_ALLOC(h->fsync, kSyncWords);
 #undef POP_ALLOC
-  if ((e = cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
-  h->fused_stages = decode_fused_stages(D, cnt.n_C);
+  if ((e = cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st)) != cudaSuccess)
+    return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection
@@ -299,7 +338,7 @@ pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, voi
   if (s != POP_OK) return s;
   POP_CUDA(h, launch_partition(h->sumsq, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step,
                                h->memory, h->err, st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -312,7 +351,7 @@ pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, v
   POP_CUDA(h, cudaMemcpyAsync(h->I, importance, sizeof(float) * h->N, cudaMemcpyDeviceToDevice, st));
   POP_CUDA(h, launch_partition(nullptr, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step, h->memory,
                                h->err, st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -341,7 +380,7 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
   if (nP) POP_CUDA(h, cudaMemcpyAsync(h->P, P, sizeof(int) * nP, cudaMemcpyHostToDevice, st));
   POP_CUDA(h, cudaMemsetAsync(h->step, 0, sizeof(int), st));
   POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, 4 * sizeof(unsigned), st));
+  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
   POP_CUDA(h, cudaStreamSynchronize(st));
   h->partitioned = true;
   h->selected = false;
@@ -359,52 +398,37 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const PackedWeights w = packed(h);
   const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
-  if (B == 1 && h->fused_on && h->fused_stages > 0 && h->num_sms <= h->ypart_parts) {
-    FusedDecodeArgs a{};
-    a.Wp = h->Wp;
-    a.n2 = h->n2;
-    a.D = h->D;
-    a.N = h->N;
-    a.x = static_cast<const uint16_t*>(x);
-    a.rc = h->rc;
-    a.nC = nC;
-    a.nR = nR;
+  prof_begin(h);
+  if (B == 1) {
+    const int grid = h->num_sms * 4;
+    DecodeB1Args a = b1_args(h, static_cast<const uint16_t*>(x), y, h->rc, nC, nR);
+    a.do_select = nC <= FZ_MAX_C ? 1 : 0;
     a.k = h->cnt.k;
-    a.period = h->cfg.period;
-    a.zC = h->z;
-    a.scores = h->scores;
-    a.memory = h->memory;
-    a.S = h->S;
-    a.step = h->step;
-    a.ypart = h->ypart;
-    a.y = y;
-    a.out_f32 = h->cfg.out_f32;
-    a.sync = h->fsync;
-    a.err = h->err;
-    a.wait_ns = h->wait_ns;
-    a.stages = h->fused_stages;
-    // CTA 0 runs the top-k (a few microseconds) and gives up about 180 KB of R rows for it
-    a.r_skew = static_cast<int>((180 * 1024 + 6 * h->D - 1) / (6 * h->D));
+    a.kd = h->cnt.k;
     prof_mark(h, 0, st);
-    POP_CUDA(h, launch_decode_fused_b1(a, h->num_sms, st));
-    for (int i = 1; i < kProfEvents; ++i) prof_mark(h, i, st);
-    if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps) ++h->prof_steps;
-    h->selected = true;
-    return POP_OK;
-  }
-  prof_mark(h, 0, st);
-  POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
+    POP_CUDA(h, launch_gateup_sel_b1(a, grid, st));
+    prof_mark(h, 1, st);
+    if (!a.do_select)
+      POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+    prof_mark(h, 2, st);
+    POP_CUDA(h, launch_down_tiled_b1(a, h->num_sms, st));
+    prof_mark(h, 3, st);
+    prof_mark(h, 4, st);
+  } else {
+    prof_mark(h, 0, st);
+    POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
+                                     h->err, h->num_sms, st));
+    prof_mark(h, 1, st);
+    POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+    prof_mark(h, 2, st);
+    int G = 0;
+    POP_CUDA(h, launch_down_decode(w, h->rc, nC, nR, h->S, h->cnt.k, h->z, nRC, B, h->ypart, h->ypart_parts / B, &G,
                                    h->err, h->num_sms, st));
-  prof_mark(h, 1, st);
-  POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
-  prof_mark(h, 2, st);
-  int G = 0;
-  POP_CUDA(h, launch_down_decode(w, h->rc, nC, nR, h->S, h->cnt.k, h->z, nRC, B, h->ypart,
-                                 h->ypart_parts / (B == 1 ? 1 : B), &G, h->err, h->num_sms, st));
-  prof_mark(h, 3, st);
-  POP_CUDA(h, launch_reduce_y(h->ypart, G, B, h->D, y, h->cfg.out_f32, st));
-  prof_mark(h, 4, st);
-  if (!h->prof_events.empty() && h->prof_steps < kProfMaxSteps) ++h->prof_steps;
+    prof_mark(h, 3, st);
+    POP_CUDA(h, launch_reduce_y(h->ypart, G, B, h->D, y, h->cfg.out_f32, st));
+    prof_mark(h, 4, st);
+  }
+  prof_end(h);
   h->selected = true;
   return POP_OK;
 }
@@ -416,6 +440,12 @@ pop_status pop_ffn_dense_ref(pop_ffn_t h, const void* X, int M, void* Y, void* s
     return fail(h, POP_ERR_INVALID_ARG, "pop_ffn_dense_ref: X, Y must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (M > h->cfg.max_batch) return prefill_gemms(h, static_cast<const uint16_t*>(X), M, Y, false, st);
+  if (M == 1) {
+    DecodeB1Args a = b1_args(h, static_cast<const uint16_t*>(X), Y, h->idx_all, 0, h->N);
+    POP_CUDA(h, launch_gateup_sel_b1(a, h->num_sms * 4, st));
+    POP_CUDA(h, launch_down_tiled_b1(a, h->num_sms, st));
+    return POP_OK;
+  }
   const PackedWeights w = packed(h);
   POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, h->z, h->N, h->scores,
                                    h->err, h->num_sms, st));
@@ -477,20 +507,12 @@ pop_status pop_get_step(pop_ffn_t h, int* step) {
   return POP_OK;
 }
 
-pop_status pop_set_option(pop_ffn_t h, int option, int value) {
-  if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_set_option: NULL handle");
-  if (option == POP_OPT_FUSED_DECODE) {
-    h->fused_on = value != 0;
-    return POP_OK;
-  }
-  return fail(h, POP_ERR_INVALID_ARG, "pop_set_option: unknown option");
-}
-
 pop_status pop_profile_enable(pop_ffn_t h, int enable) {
   if (!h) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_profile_enable: NULL handle");
   POP_CUDA(h, cudaDeviceSynchronize());
   destroy_events(h);
-  if (!enable) return POP_OK;
+  if (enable <= 0) return POP_OK;
+  h->prof_stride = enable;
   h->prof_events.resize(static_cast<size_t>(kProfEvents) * kProfMaxSteps);
   for (auto& e : h->prof_events) {
     cudaError_t r = cudaEventCreate(&e);
@@ -531,7 +553,7 @@ pop_status pop_check(pop_ffn_t h) {
   POP_CUDA(h, cudaMemset(h->err, 0, sizeof(unsigned)));
   char buf[200];
   std::snprintf(buf, sizeof buf,
-                "device error word 0x%x (1/2/32: prefill gate-up / prefill down / fused decode wait ran out; "
+                "device error word 0x%x (1/2/32: prefill gate-up / prefill down / decode selector wait ran out; "
                 "4: partition; 8: top-k; 16: index)", e);
   return fail(h, (e & DEVERR_TIMEOUT_ANY) ? POP_ERR_TIMEOUT : POP_ERR_DEVICE, buf);
 }

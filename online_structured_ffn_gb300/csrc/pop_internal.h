@@ -13,7 +13,7 @@ enum : unsigned {
   DEVERR_PARTITION = 1u << 2,       // partition: region sizes did not match the counts
   DEVERR_TOPK = 1u << 3,            // top-k: selected count did not match k
   DEVERR_INDEX = 1u << 4,           // an index list entry was out of range
-  DEVERR_TIMEOUT_DECODE = 1u << 5,  // fused decode step: a wait ran out
+  DEVERR_TIMEOUT_DECODE = 1u << 5,  // B = 1 decode: the selector's wait for the candidate scores ran out
   DEVERR_TIMEOUT_ANY = DEVERR_TIMEOUT_GATEUP | DEVERR_TIMEOUT_DOWN | DEVERR_TIMEOUT_DECODE,
 };
 
@@ -42,34 +42,37 @@ int down_decode_parts(int D, int B, int nitems, int num_sms);
 // y[b][d] = sum_g ypart[g][b][d] (g ascending); y is fp32 or bf16.
 cudaError_t launch_reduce_y(const float* ypart, int G, int B, int D, void* y, int out_f32, cudaStream_t st);
 
-// ---- fused decode step for B = 1 (pop_fused.cu)
-constexpr int FZ_MAX_C = 8192;  // largest |C| the fused step handles (its top-k keys sit in shared memory)
-struct FusedDecodeArgs {
+// ---- decode step for B = 1 (pop_decode1.cu): gate/up with in-kernel top-k, tiled down
+struct DecodeB1Args {
   const uint16_t* Wp;
   const float* n2;
   int D, N;
-  const uint16_t* x;  // [D] bf16
-  const int* rc;      // [C | R] channel indices
-  int nC, nR, k, period;
-  float* zC;          // [nC] z of the candidates
-  float* scores;      // [nC]
-  float* memory;      // [nC]
-  int* S;             // [k] selected positions into C
+  const uint16_t* x;   // [D] bf16
+  const int* rc;       // [C | R] channel indices (or all channels for the dense path)
+  int nC, nR;
+  int do_select;       // 1: CTA 0 of the gate/up grid runs the memory update and the top-k
+  int k;               // candidates to select
+  int kd;              // selected candidates the down projection adds (k, or 0 for the dense path)
+  int period;
+  float* z;            // [nC + nR]
+  float* scores;       // [nC]
+  float* memory;       // [nC]
+  int* S;              // [k] positions into C
   int* step;
-  float* ypart;       // [grid][D] partial sums
+  float* ypart;        // [chunks][D]
   void* y;
   int out_f32;
-  unsigned* sync;     // 4 counters, all 0 before the first launch: C arrivals, selection generation,
-                      // grid-barrier arrivals, grid-barrier generation
+  unsigned* sync;      // 1 counter: candidates scored so far (0 between launches)
+  unsigned* tile_cnt;  // per 512-wide tile of y: chunk CTAs done (0 between launches)
   unsigned* err;
   uint64_t wait_ns;
-  int stages;         // ring stages of 6*D bytes
-  int r_skew;         // R channels CTA 0 gives up to make room for the top-k
 };
-// Stages that fit for (D, |C|), or 0 when the fused step cannot run those sizes.
-int decode_fused_stages(int D, int nC);
-size_t decode_fused_smem(int D, int nC, int stages);
-cudaError_t launch_decode_fused_b1(const FusedDecodeArgs& a, int num_sms, cudaStream_t st);
+int down_tiled_chunks(int D, int nitems, int num_sms);
+cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st);
+cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st);
+
+// largest |C| whose top-k runs inside the B = 1 gate/up kernel (its keys sit in shared memory)
+constexpr int FZ_MAX_C = 8192;
 
 // ---- selection (pop_select.cu)
 // Importance from channel sums (if sumsq != NULL: I = n2 * sqrt(sumsq), written to I), then the

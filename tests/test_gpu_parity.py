@@ -156,14 +156,14 @@ def test_decode_parity_shapes(env, D, N):
     lay.close()
 
 
-@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("D,N,r,gamma,period", [(512, 2048, 0.3, 0.1, 1), (4096, 11008, 0.299, 0.1, 1),
                                                 (256, 1024, 0.5, 0.1, 4), (1024, 600, 0.3, 0.0, 1),
-                                                (1024, 600, 0.4, 0.6, 1), (2048, 333, 0.0, 0.1, 1)])
-def test_single_token_paths(env, fused, D, N, r, gamma, period):
-    # B = 1 runs as one persistent kernel by default; the four-kernel path is the other option.
+                                                (1024, 600, 0.4, 0.6, 1), (2048, 333, 0.0, 0.1, 1),
+                                                (256, 20000, 0.4, 0.6, 1), (256, 20000, 0.5, 0.5, 3)])
+def test_single_token_paths(env, D, N, r, gamma, period):
+    # B = 1: the top-k runs inside the gate/up kernel for |C| <= 8192 and as its own kernel above
+    # (the last two shapes have |C| = 20000).
     lay = Layer(env, D, N, r=r, gamma=gamma, period=period)
-    lay.ffn.set_fused_decode(fused)
     Wg, W1, W2 = lay.w64()
     ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 8, lay.sc)), r, gamma)
     if period == 1:
@@ -187,8 +187,8 @@ def test_single_token_paths(env, fused, D, N, r, gamma, period):
     lay.close()
 
 
-def test_fused_step_is_repeatable(env):
-    # the persistent kernel reduces its partial sums in a fixed order: identical runs, identical y
+def test_decode_step_is_repeatable(env):
+    # partial sums are reduced in a fixed order: identical runs give identical y
     _, torch, dev = env
     D, N = 1024, 4096
     a = Layer(env, D, N, r=0.3, gamma=0.1)
