@@ -162,7 +162,7 @@ pop_status pop_set_wait_limit(pop_ffn_t h, uint64_t ns);
 
 /* Per-kernel timing of decode steps (off by default). enable = n >= 1: one pop_decode_step in
  * every n records CUDA events on its stream between its kernel slots (gate/up, selection, down,
- * reduction; a slot a path does not launch reads near zero), for up to 4096 timed steps between
+ * reduction; a slot a path does not launch reads near zero), for up to 256 timed steps between
  * reads. Each event adds a little GPU time, which sampling keeps out of most steps.
  * enable = 0 turns timing off. Enabling creates the events; disabling destroys them. */
 pop_status pop_profile_enable(pop_ffn_t h, int enable);

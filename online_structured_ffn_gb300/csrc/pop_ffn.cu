@@ -57,7 +57,7 @@ struct pop_ffn {
 static constexpr int kProfEvents = 5;
 // device counters: [4] candidates scored by the B = 1 gate/up, [8..] tiles of y done by the down chunks
 static constexpr int kSyncWords = 64;
-static constexpr int kProfMaxSteps = 4096;
+static constexpr int kProfMaxSteps = 256;
 
 namespace {
 thread_local std::string g_msg;

@@ -20,12 +20,21 @@ namespace pop {
 constexpr int RADIX_BITS = 11;
 constexpr int RADIX_BINS = 1 << RADIX_BITS;
 
+// keys of the cut-off bin that the top-k ranks directly
+constexpr int SEL_GATHER = 256;
+
 template <int NTH>
 struct RadixScratch {
+  static_assert(NTH >= 64 && RADIX_BINS % NTH == 0, "whole warps, bins split evenly");
   uint32_t hist[RADIX_BINS];
   uint32_t wsum[NTH / 32];
   uint32_t bcast[4];
   uint32_t warp_tot[NTH / 32][3];
+  uint32_t wmin[NTH / 32], wmax[NTH / 32], wcnt[NTH / 32];
+  uint32_t gcnt;
+  int gsel;
+  uint32_t gkey[SEL_GATHER];
+  int gidx[SEL_GATHER];
 };
 
 // Block-wide exclusive scan of one value per thread (thread order); returns the total.
@@ -227,37 +236,177 @@ __device__ void block_scan3(int tid, const uint32_t (&c)[3], uint32_t (&excl)[3]
 // Top-k of one decode step over n candidate keys (optionally accumulating the periodic memory):
 // writes the k selected positions, ascending, to S. Returns false if the count came out wrong.
 // keys must hold n entries. score(i) is the candidate's score for this step.
+//
+// The cut-off is found in one histogram pass: the top RADIX_BITS occupied bits of the key offsets
+// split the keys into bins, a scan finds the bin holding the cut-off position, and, when that bin
+// holds at most SEL_GATHER keys (the usual case: a few), its keys are gathered and ranked directly
+// under the (key ascending, index descending) order. A fuller bin takes the general order statistic.
+// The selected positions are written in ascending order by a warp-ballot compaction. Seven
+// barriers in all on the usual path.
 template <int NTH, class Sync, class Score>
 __device__ bool select_step(int tid, Score score, float* memory, int n, int k, int period, bool update,
                             uint32_t* keys, int* S, RadixScratch<NTH>& sc, Sync sync) {
-  for (int i = tid; i < n; i += NTH) {
-    float v = score(i);
-    if (period > 1) {
-      v += memory[i];
-      memory[i] = update ? 0.f : v;
+  constexpr int NW = NTH / 32;
+  constexpr int U = 8;
+  const int lane = tid & 31, warp = tid >> 5;
+  const bool topk = update && k > 0;
+  // fill the keys (and the memory); the whole-range bounds and the cleared histogram come with them
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int base = tid; base < n; base += NTH * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NTH;
+      v[u] = i < n ? score(i) : 0.f;
     }
-    keys[i] = float_key(v);
+    if (period > 1) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * NTH;
+        if (i < n) {
+          v[u] += memory[i];
+          memory[i] = update ? 0.f : v[u];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NTH;
+      if (i < n) {
+        const uint32_t kv = float_key(v[u]);
+        keys[i] = kv;
+        lo = min(lo, kv);
+        hi = max(hi, kv);
+      }
+    }
   }
-  sync();
-  if (!update || k <= 0) return true;
+  if (topk && k < n) {
+    for (int b = tid; b < RADIX_BINS; b += NTH) sc.hist[b] = 0u;
+    if (tid == 0) sc.gcnt = 0u;
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+      sc.wmin[warp] = lo;
+      sc.wmax[warp] = hi;
+    }
+  }
+  sync();  // barrier 1
+  if (!topk) return true;
   uint32_t vS = 0;
   int jS = n;
-  if (k < n) order_statistic<NTH>(tid, keys, n, static_cast<uint32_t>(n - k), sc, sync, vS, jS);
-  const int per = (n + NTH - 1) / NTH;
-  const int i0 = min(n, tid * per);
-  const int i1 = min(n, i0 + per);
+  if (k < n) {
+    lo = 0xffffffffu;
+    hi = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      lo = min(lo, sc.wmin[w]);
+      hi = max(hi, sc.wmax[w]);
+    }
+    const uint32_t t = static_cast<uint32_t>(n - k);  // ascending position of the cut-off
+    if (hi == lo) {
+      // one key value: ascending order is descending index, position t is index n - 1 - t
+      vS = lo;
+      jS = k - 1;
+    } else {
+      const int bits = 32 - __clz(hi - lo);
+      const int shift = bits > RADIX_BITS ? bits - RADIX_BITS : 0;
+      for (int i = tid; i < n; i += NTH) atomicAdd(&sc.hist[(keys[i] - lo) >> shift], 1u);
+      sync();  // barrier 2
+      constexpr int PER = RADIX_BINS / NTH;
+      uint32_t run = 0;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) run += sc.hist[tid * PER + j];
+      uint32_t incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) sc.wsum[warp] = incl;
+      sync();  // barrier 3
+      uint32_t before = incl - run;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) before += w < warp ? sc.wsum[w] : 0u;
+      if (t >= before && t < before + run) {
+        uint32_t acc = before;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const uint32_t c = sc.hist[tid * PER + j];
+          if (t >= acc && t < acc + c) {
+            sc.bcast[0] = static_cast<uint32_t>(tid * PER + j);
+            sc.bcast[1] = acc;
+            sc.bcast[2] = c;
+          }
+          acc += c;
+        }
+      }
+      sync();  // barrier 4
+      const uint32_t bin = sc.bcast[0], below = sc.bcast[1], cnt = sc.bcast[2];
+      if (cnt <= static_cast<uint32_t>(SEL_GATHER)) {
+        for (int i = tid; i < n; i += NTH) {
+          const uint32_t kv = keys[i];
+          if (((kv - lo) >> shift) == bin) {
+            const uint32_t slot = atomicAdd(&sc.gcnt, 1u);
+            if (slot < static_cast<uint32_t>(SEL_GATHER)) {
+              sc.gkey[slot] = kv;
+              sc.gidx[slot] = i;
+            }
+          }
+        }
+        sync();  // barrier 5
+        const uint32_t want = t - below;
+        for (uint32_t s = tid; s < cnt; s += NTH) {
+          const uint32_t kv = sc.gkey[s];
+          const int iv = sc.gidx[s];
+          uint32_t rank = 0;
+          for (uint32_t m = 0; m < cnt; ++m) {
+            const uint32_t km = sc.gkey[m];
+            rank += (km < kv || (km == kv && sc.gidx[m] > iv)) ? 1u : 0u;
+          }
+          if (rank == want) {
+            sc.bcast[3] = kv;
+            sc.gsel = iv;
+          }
+        }
+        sync();  // barrier 6
+        vS = sc.bcast[3];
+        jS = sc.gsel;
+      } else {
+        uint32_t v;
+        order_statistic<NTH>(tid, keys, n, t, sc, sync, v, jS);
+        vS = v;
+      }
+    }
+  }
+  // ascending compaction: warp w owns a contiguous run of whole 32-key groups
+  const int groups = (n + 31) / 32;
+  const int g0 = warp * groups / NW, g1 = (warp + 1) * groups / NW;
   auto sel = [&](int i) {
+    if (i >= n) return false;
     if (k >= n) return true;
     const uint32_t kv = keys[i];
     return kv > vS || (kv == vS && i <= jS);
   };
-  uint32_t c[3] = {0, 0, 0};
-  for (int i = i0; i < i1; ++i) c[0] += sel(i) ? 1u : 0u;
-  uint32_t off[3], tot[3];
-  block_scan3<NTH>(tid, c, off, tot, sc, sync);
-  if (tot[0] != static_cast<uint32_t>(k)) return false;
-  for (int i = i0; i < i1; ++i)
-    if (sel(i)) S[off[0]++] = i;
+  uint32_t mine = 0;
+  for (int g = g0; g < g1; ++g) mine += __popc(__ballot_sync(0xffffffffu, sel(32 * g + lane)));
+  if (lane == 0) sc.wcnt[warp] = mine;
+  sync();  // barrier 7
+  uint32_t off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const uint32_t c = sc.wcnt[w];
+    off += w < warp ? c : 0u;
+    tot += c;
+  }
+  if (tot != static_cast<uint32_t>(k)) return false;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int g = g0; g < g1; ++g) {
+    const int i = 32 * g + lane;
+    const bool b = sel(i);
+    const uint32_t m = __ballot_sync(0xffffffffu, b);
+    if (b) S[off + __popc(m & lt_mask)] = i;
+    off += __popc(m);
+  }
   return true;
 }
 
