@@ -15,13 +15,16 @@
 // Launch 2, k_down_tiled_b1: y = sum over R u S of z_i W2[:, i]. CTA (t, c) owns the 512-wide
 // tile t of y and the c-th chunk of the kept channels; 8 groups of 64 threads each read one
 // channel's 1 KB slice of the contiguous down column with 16-byte loads. The last chunk CTA to
-// finish a tile (atomic counter) adds the chunks' partial tiles in chunk order: no extra launch,
-// and the result does not depend on timing.
+// finish a tile (atomic counter) adds the chunks' partial tiles in a fixed order: no extra
+// launch, and the result does not depend on timing.
 //
-// Both kernels are launched with programmatic dependent launch when the caller's stream allows it:
-// before waiting for the previous kernel (griddepcontrol.wait) they only prefetch weight rows into
-// L2 (constant data); they read x, z and S and write z, S, y only after the wait, so the overlap
-// with the previous kernel's tail never races on data.
+// Both kernels are launched with programmatic dependent launch when the caller's stream allows it.
+// Before waiting for the previous kernel (griddepcontrol.wait) they touch constant data only: L2
+// prefetches of weight rows, and in the down kernel the channel ids of R, which only a partition
+// changes; a partition is written by ordinary launches that have completed before the gate/up
+// grid passes its wait, and the gate/up grid lets the down grid start only after that wait. x, z
+// and S are read and z, S, y written only after the wait, so the overlap with the previous
+// kernel's tail never races on data.
 #include "pop_device.cuh"
 #include "pop_internal.h"
 #include "pop_radix.cuh"
@@ -56,6 +59,16 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// One atomic that publishes this CTA's earlier writes (ordered before it by a CTA barrier) and,
+// for the caller that sees the final count, makes the other CTAs' published writes visible.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -73,8 +86,8 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
 
   if (cta == 0) {
     // ---------------------------------------------------------------- selector
-    pdl_trigger();  // the next kernel may take free SM slots; it waits for this grid before using S
     pdl_wait();     // S, memory and step may still be read by the previous step's kernels
+    pdl_trigger();  // the next kernel may take free SM slots; it waits for this grid before using S
     if (a.do_select) {
       if (threadIdx.x == 0) {
         bool ok = true;
@@ -132,8 +145,8 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
       }
     }
   }
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();  // after the wait: the partition this grid reads is then complete for the next grid too
   for (int c = threadIdx.x; c < nch; c += GS_THREADS) {
     const uint4 v = *reinterpret_cast<const uint4*>(a.x + 8 * c);
     reinterpret_cast<float4*>(xs + 8 * c)[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
@@ -200,10 +213,7 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
   };
 
   for (int p = c0; p < c1; ++p) item(p);
-  if (a.do_select && c1 > c0 && lane == 0) {
-    __threadfence();
-    atomicAdd(a.sync, static_cast<unsigned>(c1 - c0));
-  }
+  if (a.do_select && c1 > c0 && lane == 0) red_add_release(a.sync, static_cast<unsigned>(c1 - c0));
   for (int p = r0; p < r1; ++p) item(p);
 }
 
@@ -217,33 +227,49 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   const int grp = threadIdx.x / (DT_TILE / 8), tt = threadIdx.x % (DT_TILE / 8);
   const int d = tile * DT_TILE + 8 * tt;
   const bool dok = d < D;
-  const long long n = static_cast<long long>(a.nR) + a.kd;
-  const int i0 = static_cast<int>(chunk * n / NCK), i1 = static_cast<int>((chunk + 1) * n / NCK);
+  // chunk c takes the c-th share of R and the c-th share of S, so every CTA has the same mix of
+  // prefetched (R) and not prefetched (S) columns
+  const int r_lo = static_cast<int>(static_cast<long long>(chunk) * a.nR / NCK);
+  const int nr = static_cast<int>(static_cast<long long>(chunk + 1) * a.nR / NCK) - r_lo;
+  const int s_lo = static_cast<int>(static_cast<long long>(chunk) * a.kd / NCK);
+  const int ns = static_cast<int>(static_cast<long long>(chunk + 1) * a.kd / NCK) - s_lo;
+  const int n_items = nr + ns;  // item e < nr is R item r_lo + e, else S item s_lo + e - nr
   const size_t row3 = 3 * static_cast<size_t>(D);
+  const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(D);  // down part of packed row 0
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  // constant data only before the wait: warm L2 with this CTA's slices of the retained channels'
-  // down columns (one thread per 128-byte line)
-  if (dok && (tt & 7) == 0) {
-    const int rlim = min(i1, a.nR);
-    for (int it = i0 + grp; it < rlim; it += DT_GROUPS) {
-      const int ch = a.rc[a.nC + it];
-      if (static_cast<unsigned>(ch) < static_cast<unsigned>(a.N))
-        prefetch_l2(a.Wp + static_cast<size_t>(ch) * row3 + 2 * static_cast<size_t>(D) + d);
+  // Constant data only before the wait: the channel ids of the first batch's retained items (R
+  // never changes between partitions, and a partition is written by an ordinary launch that has
+  // finished before this grid's primary started), and an L2 prefetch of their down slices, one
+  // 128-byte line per thread and round.
+  const int nr0 = min(DT_BATCH, nr);
+  for (int e = threadIdx.x; e < nr0; e += DT_THREADS) s_ch[e] = guard_idx(__ldcg(a.rc + a.nC + r_lo + e), a.N, a.err);
+  __syncthreads();
+  {
+    constexpr int LPS = DT_TILE * 2 / 128;  // 128-byte lines per tile slice
+    for (int q = threadIdx.x; q < nr0 * LPS; q += DT_THREADS) {
+      const int dd = tile * DT_TILE + (q % LPS) * 64;
+      if (dd < D) prefetch_l2(W2 + static_cast<size_t>(s_ch[q / LPS]) * row3 + dd);
     }
   }
   pdl_trigger();
   pdl_wait();
 
-  for (int base = i0; base < i1; base += DT_BATCH) {
-    const int cnt = min(DT_BATCH, i1 - base);
-    __syncthreads();
+  for (int base = 0; base < n_items; base += DT_BATCH) {
+    const int cnt = min(DT_BATCH, n_items - base);
+    const bool first = base == 0;
+    if (!first) __syncthreads();
     for (int e = threadIdx.x; e < cnt; e += DT_THREADS) {
       const int it = base + e;
-      const int pos = it < a.nR ? a.nC + it : guard_idx(a.S[it - a.nR], a.nC, a.err);
-      s_ch[e] = guard_idx(a.rc[pos], a.N, a.err);
-      s_z[e] = a.z[pos];
+      if (it < nr) {
+        if (!first) s_ch[e] = guard_idx(a.rc[a.nC + r_lo + it], a.N, a.err);
+        s_z[e] = a.z[a.nC + r_lo + it];
+      } else {
+        const int pos = guard_idx(a.S[s_lo + it - nr], a.nC, a.err);
+        s_ch[e] = guard_idx(a.rc[pos], a.N, a.err);
+        s_z[e] = a.z[pos];
+      }
     }
     __syncthreads();
     for (int ii = grp; ii < cnt; ii += DT_GROUPS * DT_UNROLL) {
@@ -253,8 +279,7 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
       for (int u = 0; u < DT_UNROLL; ++u) {
         const int idx = ii + DT_GROUPS * u;
         const bool ok = idx < cnt && dok;
-        v[u] = ok ? ldg_stream(a.Wp + static_cast<size_t>(s_ch[idx]) * row3 + 2 * static_cast<size_t>(D) + d)
-                  : make_uint4(0u, 0u, 0u, 0u);
+        v[u] = ok ? ldg_stream(W2 + static_cast<size_t>(s_ch[idx]) * row3 + d) : make_uint4(0u, 0u, 0u, 0u);
         zz[u] = idx < cnt ? s_z[idx] : 0.f;
       }
 #pragma unroll
@@ -280,16 +305,36 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
     for (int g = 0; g < DT_GROUPS; ++g) s += red[g][threadIdx.x];
     a.ypart[static_cast<size_t>(chunk) * D + e] = s;
   }
-  __threadfence();
+  // release this chunk's partial tile; the last chunk CTA of the tile adds all of them
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.tile_cnt + tile, 1u) == static_cast<unsigned>(NCK) - 1u;
+  if (threadIdx.x == 0) s_last = atom_add_acq_rel(a.tile_cnt + tile, 1u) == static_cast<unsigned>(NCK) - 1u;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  // DT_THREADS / (DT_TILE / 4) subsets of the chunks, each summed in chunk order over float4
+  // columns, then the subsets in order: a fixed order, so y does not depend on timing.
+  constexpr int QPT = DT_TILE / 4;             // float4 columns of the tile
+  constexpr int NSUB = DT_THREADS / QPT;       // chunk subsets
+  static_assert(NSUB * QPT == DT_THREADS && NSUB <= DT_GROUPS, "tile reduction layout");
+  const int qc = threadIdx.x % QPT, sub = threadIdx.x / QPT;
+  const int e4 = tile * DT_TILE + 4 * qc;
+  float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (e4 < D) {
+    // D is a multiple of 8, so a float4 column inside y lies wholly inside it
+#pragma unroll 8
+    for (int c = sub; c < NCK; c += NSUB) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ypart + static_cast<size_t>(c) * D + e4));
+      t4.x += v.x;
+      t4.y += v.y;
+      t4.z += v.z;
+      t4.w += v.w;
+    }
+  }
+  reinterpret_cast<float4*>(&red[sub][0])[qc] = t4;
+  __syncthreads();
   if (threadIdx.x < DT_TILE && e < D) {
     float t = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < NCK; ++c) t += __ldcg(a.ypart + static_cast<size_t>(c) * D + e);
+#pragma unroll
+    for (int g = 0; g < NSUB; ++g) t += red[g][threadIdx.x];
     if (a.out_f32)
       static_cast<float*>(a.y)[e] = t;
     else

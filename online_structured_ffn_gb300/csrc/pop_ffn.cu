@@ -37,8 +37,14 @@ struct pop_ffn {
   float* scores = nullptr;
   float* memory = nullptr;
   int* S = nullptr;
-  float* ypart = nullptr;
-  int ypart_parts = 0;  // capacity in units of D floats
+  float* ypart = nullptr;  // B = 1 down: partial tiles [chunks][D]
+  int ypart_parts = 0;     // capacity in units of D floats
+  // B > 1 decode (tensor-core kernels)
+  uint16_t* zk = nullptr;  // [2][max_batch][ldk]: bf16 hi and lo parts of z of the kept items (R, then S)
+  int ldk = 0;
+  int* ch_list = nullptr;  // kept item -> channel
+  float* ws = nullptr;     // stream-K partial accumulators
+  unsigned* tc_cnt = nullptr;  // per-tile counters: [0, kTcDownCnt) gate/up, [kTcDownCnt, ..) down
   int* step = nullptr;
   unsigned* err = nullptr;
   unsigned* fsync = nullptr;  // inter-CTA counters of the decode kernels
@@ -58,6 +64,9 @@ static constexpr int kProfEvents = 5;
 // device counters: [4] candidates scored by the B = 1 gate/up, [8..] tiles of y done by the down chunks
 static constexpr int kSyncWords = 64;
 static constexpr int kProfMaxSteps = 256;
+// stream-K tile counters of the B > 1 kernels: gate/up tiles (<= D_FF / 128) first, then down tiles (<= D / 128)
+static constexpr int kTcDownCnt = (POP_MAX_D_FF + 127) / 128;
+static constexpr int kTcCntWords = kTcDownCnt + (POP_MAX_D + 127) / 128;
 
 namespace {
 thread_local std::string g_msg;
@@ -90,8 +99,6 @@ cudaError_t dalloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
 }
 
-PackedWeights packed(const pop_ffn* h) { return PackedWeights{h->Wp, h->n2, h->D, h->N}; }
-
 void destroy_events(pop_ffn* h) {
   for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
   h->prof_events.clear();
@@ -115,8 +122,9 @@ void prof_end(pop_ffn* h) {
 }
 
 void free_all(pop_ffn* h) {
-  void* ptrs[] = {h->Wp, h->n2, h->Z, h->part, h->sumsq, h->I, h->rc, h->P, h->idx_all,
-                  h->z,  h->scores, h->memory, h->S, h->ypart, h->step, h->err, h->fsync};
+  void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
+                  h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_list,
+                  h->ws,    h->tc_cnt, h->step, h->err,     h->fsync};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -145,6 +153,74 @@ DecodeB1Args b1_args(pop_ffn* h, const uint16_t* x, void* y, const int* rc, int 
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   return a;
+}
+
+// Zeroes every inter-CTA counter of the decode kernels (they are left at zero by each launch that
+// completes, so this only matters after a partition change or a reported device error).
+cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
+  if (e == cudaSuccess && h->tc_cnt) e = cudaMemsetAsync(h->tc_cnt, 0, kTcCntWords * sizeof(unsigned), st);
+  return e;
+}
+
+// gate/up over positions [0, nRC) of rc for B tokens: z, zk (positions >= nC) and scores (< nC).
+pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nRC, int nC, cudaStream_t st) {
+  DecodeTcArgs a{};
+  a.Wp = h->Wp;
+  a.D = h->D;
+  a.B = B;
+  a.NP = round_up(B, 16);
+  a.rows = nRC;
+  a.K = h->D;
+  a.N = h->N;
+  a.rc = rc;
+  a.nC = nC;
+  a.n2 = h->n2;
+  a.z = h->z;
+  a.ldz = nRC;
+  a.zk = h->zk;
+  a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
+  a.ldk = h->ldk;
+  a.scores = h->scores;
+  a.ws = h->ws;
+  a.tile_cnt = h->tc_cnt;
+  a.err = h->err;
+  a.wait_ns = h->wait_ns;
+  CUtensorMap xm;
+  if (!encode_tokens_map(&xm, x, h->D, B, h->D, a.NP))
+    return fail(h, POP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed for x");
+  POP_CUDA(h, launch_gateup_tc(xm, a, h->num_sms, st));
+  return POP_OK;
+}
+
+// y[b] = sum over the nK kept items j of zk[b][j] * W2[:, ch_list[j]] for B tokens.
+pop_status down_tc(pop_ffn* h, int B, const int* ch_list, int nK, void* y, cudaStream_t st) {
+  if (nK <= 0) {
+    const size_t bytes = static_cast<size_t>(B) * h->D * (h->cfg.out_f32 ? 4 : 2);
+    POP_CUDA(h, cudaMemsetAsync(y, 0, bytes, st));
+    return POP_OK;
+  }
+  DecodeTcArgs a{};
+  a.Wp = h->Wp;
+  a.D = h->D;
+  a.B = B;
+  a.NP = round_up(B, 16);
+  a.rows = h->D;
+  a.K = nK;
+  a.N = h->N;
+  a.ch_list = ch_list;
+  a.y = y;
+  a.out_f32 = h->cfg.out_f32;
+  a.ws = h->ws;
+  a.tile_cnt = h->tc_cnt + kTcDownCnt;
+  a.err = h->err;
+  a.wait_ns = h->wait_ns;
+  CUtensorMap zm, zlm;
+  if (!encode_tokens_map(&zm, h->zk, nK, B, h->ldk, a.NP) ||
+      !encode_tokens_map(&zlm, h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, nK, B, h->ldk, a.NP))
+    return fail(h, POP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed for z");
+  POP_CUDA(h, launch_down_tc(zm, zlm, a, h->num_sms, st));
+  return POP_OK;
 }
 
 __global__ void k_iota(int* a, int n) {
@@ -233,8 +309,8 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   h->Mcap = round_up(cfg->max_prefill_tokens, 128);
   h->ldZ = round_up(N, 128);
   h->ldPart = h->ldZ;
-  const int gk = down_decode_parts(D, 2, 1 << 30, h->num_sms);
-  h->ypart_parts = std::max(2 * h->num_sms, gk * cfg->max_batch);
+  h->ypart_parts = 2 * h->num_sms;
+  h->ldk = round_up(N, 8);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   auto bail = [&](cudaError_t err, const char* where) {
@@ -261,6 +337,12 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->memory, N);
   POP_ALLOC(h->S, N);
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
+  if (cfg->max_batch > 1) {
+    POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
+    POP_ALLOC(h->ch_list, N);
+    POP_ALLOC(h->ws, decode_tc_workspace_floats(h->num_sms));
+    POP_ALLOC(h->tc_cnt, kTcCntWords);
+  }
   POP_ALLOC(h->step, 1);
   POP_ALLOC(h->err, 1);
   POP_ALLOC(h->fsync, kSyncWords);
@@ -268,6 +350,10 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   if ((e = cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st)) != cudaSuccess)
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  if (h->tc_cnt && (e = cudaMemsetAsync(h->tc_cnt, 0, kTcCntWords * sizeof(unsigned), st)) != cudaSuccess)
+    return bail(e, "cudaMemsetAsync");
+  if (h->ch_list && (e = cudaMemsetAsync(h->ch_list, 0, sizeof(int) * N, st)) != cudaSuccess)
+    return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection
   if ((e = cudaMemsetAsync(h->S, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
@@ -338,7 +424,7 @@ pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, voi
   if (s != POP_OK) return s;
   POP_CUDA(h, launch_partition(h->sumsq, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step,
                                h->memory, h->err, st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
+  POP_CUDA(h, reset_counters(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -351,7 +437,7 @@ pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, v
   POP_CUDA(h, cudaMemcpyAsync(h->I, importance, sizeof(float) * h->N, cudaMemcpyDeviceToDevice, st));
   POP_CUDA(h, launch_partition(nullptr, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step, h->memory,
                                h->err, st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
+  POP_CUDA(h, reset_counters(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -380,7 +466,7 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
   if (nP) POP_CUDA(h, cudaMemcpyAsync(h->P, P, sizeof(int) * nP, cudaMemcpyHostToDevice, st));
   POP_CUDA(h, cudaMemsetAsync(h->step, 0, sizeof(int), st));
   POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
-  POP_CUDA(h, cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st));
+  POP_CUDA(h, reset_counters(h, st));
   POP_CUDA(h, cudaStreamSynchronize(st));
   h->partitioned = true;
   h->selected = false;
@@ -396,7 +482,6 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: x, y must be 16-byte aligned");
   if (!h->partitioned) return fail(h, POP_ERR_STATE, "pop_decode_step: no partition (run a prefill first)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const PackedWeights w = packed(h);
   const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
   prof_begin(h);
   if (B == 1) {
@@ -415,17 +500,20 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     prof_mark(h, 3, st);
     prof_mark(h, 4, st);
   } else {
+    const int nK = nR + h->cnt.k;
     prof_mark(h, 0, st);
-    POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, h->z, nRC, h->scores,
-                                     h->err, h->num_sms, st));
+    if (nRC > 0) {
+      pop_status s = gateup_tc(h, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, st);
+      if (s != POP_OK) return s;
+    }
     prof_mark(h, 1, st);
-    POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+    POP_CUDA(h, launch_select_bn(h->scores, h->memory, nC, nR, h->cnt.k, h->cfg.period, h->step, h->S, h->rc,
+                                 h->ch_list, h->z, nRC, B, h->zk,
+                                 h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, h->ldk, h->N, h->err, st));
     prof_mark(h, 2, st);
-    int G = 0;
-    POP_CUDA(h, launch_down_decode(w, h->rc, nC, nR, h->S, h->cnt.k, h->z, nRC, B, h->ypart, h->ypart_parts / B, &G,
-                                   h->err, h->num_sms, st));
+    pop_status s = down_tc(h, B, h->ch_list, nK, y, st);
+    if (s != POP_OK) return s;
     prof_mark(h, 3, st);
-    POP_CUDA(h, launch_reduce_y(h->ypart, G, B, h->D, y, h->cfg.out_f32, st));
     prof_mark(h, 4, st);
   }
   prof_end(h);
@@ -446,14 +534,10 @@ pop_status pop_ffn_dense_ref(pop_ffn_t h, const void* X, int M, void* Y, void* s
     POP_CUDA(h, launch_down_tiled_b1(a, h->num_sms, st));
     return POP_OK;
   }
-  const PackedWeights w = packed(h);
-  POP_CUDA(h, launch_gateup_decode(w, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, h->z, h->N, h->scores,
-                                   h->err, h->num_sms, st));
-  int G = 0;
-  POP_CUDA(h, launch_down_decode(w, h->idx_all, 0, h->N, h->S, 0, h->z, h->N, M, h->ypart,
-                                 h->ypart_parts / (M == 1 ? 1 : M), &G, h->err, h->num_sms, st));
-  POP_CUDA(h, launch_reduce_y(h->ypart, G, M, h->D, Y, h->cfg.out_f32, st));
-  return POP_OK;
+  // 2 <= M <= max_batch: the decode kernels over every channel (all positions count as retained)
+  pop_status s = gateup_tc(h, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, st);
+  if (s != POP_OK) return s;
+  return down_tc(h, M, h->idx_all, h->N, Y, st);
 }
 
 pop_status pop_get_partition(pop_ffn_t h, int* R, int* C, int* P) {
@@ -551,10 +635,12 @@ pop_status pop_check(pop_ffn_t h) {
   POP_CUDA(h, cudaMemcpy(&e, h->err, sizeof(unsigned), cudaMemcpyDeviceToHost));
   if (e == 0) return POP_OK;
   POP_CUDA(h, cudaMemset(h->err, 0, sizeof(unsigned)));
-  char buf[200];
+  POP_CUDA(h, reset_counters(h, nullptr));
+  POP_CUDA(h, cudaDeviceSynchronize());
+  char buf[240];
   std::snprintf(buf, sizeof buf,
-                "device error word 0x%x (1/2/32: prefill gate-up / prefill down / decode selector wait ran out; "
-                "4: partition; 8: top-k; 16: index)", e);
+                "device error word 0x%x (1/2/32/64: prefill gate-up / prefill down / decode selector / decode "
+                "tensor-core wait ran out; 4: partition; 8: top-k; 16: index)", e);
   return fail(h, (e & DEVERR_TIMEOUT_ANY) ? POP_ERR_TIMEOUT : POP_ERR_DEVICE, buf);
 }
 

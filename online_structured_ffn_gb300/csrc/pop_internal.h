@@ -14,33 +14,51 @@ enum : unsigned {
   DEVERR_TOPK = 1u << 3,            // top-k: selected count did not match k
   DEVERR_INDEX = 1u << 4,           // an index list entry was out of range
   DEVERR_TIMEOUT_DECODE = 1u << 5,  // B = 1 decode: the selector's wait for the candidate scores ran out
-  DEVERR_TIMEOUT_ANY = DEVERR_TIMEOUT_GATEUP | DEVERR_TIMEOUT_DOWN | DEVERR_TIMEOUT_DECODE,
+  DEVERR_TIMEOUT_DECODE_TC = 1u << 6,  // B > 1 decode (tensor-core kernels): a wait ran out
+  DEVERR_TIMEOUT_ANY =
+      DEVERR_TIMEOUT_GATEUP | DEVERR_TIMEOUT_DOWN | DEVERR_TIMEOUT_DECODE | DEVERR_TIMEOUT_DECODE_TC,
 };
 
-// Packed weights: row i of Wp holds [Wg[i, 0:D] | W1[i, 0:D] | W2[0:D, i]] (3*D bf16).
-struct PackedWeights {
-  const uint16_t* Wp;
-  const float* n2;  // ||W2[:, i]||_2, fp32
-  int D;
-  int N;
-};
+// Packed weights: row i of Wp holds [Wg[i, 0:D] | W1[i, 0:D] | W2[0:D, i]] (3*D bf16); n2[i] is
+// ||W2[:, i]||_2 in fp32.
 
 // ---- pack (pop_pack.cu)
 cudaError_t launch_pack(const uint16_t* Wg, const uint16_t* W1, const uint16_t* W2, uint16_t* Wp, float* n2,
                         int D, int N, cudaStream_t st);
 
-// ---- decode (pop_decode.cu)
-// z[b * ldz + p] = z of item p (channel rc[p]) for token b; scores[p] = max_b |z| * n2 for p < nC.
-cudaError_t launch_gateup_decode(const PackedWeights& w, const uint16_t* x, int B, const int* rc, int nRC, int nC,
-                                 float* z, int ldz, float* scores, unsigned* err, int num_sms, cudaStream_t st);
-// Down projection over the items R (rc positions nC .. nC+nR-1) and the selected candidates
-// (rc positions S[0..k)); partial sums go to ypart [G][B][D]; returns G through *G_out.
-cudaError_t launch_down_decode(const PackedWeights& w, const int* rc, int nC, int nR, const int* S, int k,
-                               const float* z, int ldz, int B, float* ypart, int max_parts, int* G_out,
-                               unsigned* err, int num_sms, cudaStream_t st);
-int down_decode_parts(int D, int B, int nitems, int num_sms);
-// y[b][d] = sum_g ypart[g][b][d] (g ascending); y is fp32 or bf16.
-cudaError_t launch_reduce_y(const float* ypart, int G, int B, int D, void* y, int out_f32, cudaStream_t st);
+// ---- decode step for B > 1 (pop_decode_tc.cu): stream-K skinny GEMMs on tcgen05
+// The B operand of a decode GEMM: `rows` token rows of `inner` bf16, `ld` elements apart, box
+// {64, NP} (rows NP > `rows` read as zero).
+bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int NP);
+struct DecodeTcArgs {
+  const uint16_t* Wp;    // packed weights
+  int D;
+  int B, NP;             // tokens, and tokens padded to a multiple of 16 (the MMA's N)
+  int rows;              // M extent: positions |R u C| (gate/up) or D (down)
+  int K;                 // reduction extent: D (gate/up) or the kept items |R| + k (down)
+  int N;                 // channel count, for the index guards
+  const int* rc;         // gate/up: position -> channel ([C | R])
+  const int* ch_list;    // down: kept item -> channel (R, then S)
+  int nC;                // gate/up: positions below nC are candidates
+  const float* n2;       // ||W2[:, c]||
+  float* z;              // gate/up out: fp32 [B][ldz]
+  int ldz;
+  uint16_t* zk;          // gate/up out: z of R positions at [b][p - nC], bf16 hi part
+  uint16_t* zk_lo;       // ... and bf16 lo part z - hi
+  int ldk;
+  float* scores;         // gate/up out: [nC]
+  void* y;               // down out: [B][D], fp32 or bf16
+  int out_f32;
+  float* ws;             // stream-K partial accumulators, decode_tc_workspace_floats() floats
+  unsigned* tile_cnt;    // one counter per tile (0 between launches)
+  unsigned* err;
+  uint64_t wait_ns;
+};
+cudaError_t launch_gateup_tc(const CUtensorMap& x_map, const DecodeTcArgs& args, int num_sms, cudaStream_t st);
+// zk_map / zk_lo_map: the hi and lo bf16 planes of z over the kept items
+cudaError_t launch_down_tc(const CUtensorMap& zk_map, const CUtensorMap& zk_lo_map, const DecodeTcArgs& args,
+                           int num_sms, cudaStream_t st);
+size_t decode_tc_workspace_floats(int num_sms);
 
 // ---- decode step for B = 1 (pop_decode1.cu): gate/up with in-kernel top-k, tiled down
 struct DecodeB1Args {
@@ -83,6 +101,12 @@ cudaError_t launch_partition(const float* sumsq, const float* n2, float* I, int 
 // Candidate selection for one decode step (periodic memory, top-k, step counter).
 cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
                           unsigned* err, cudaStream_t st);
+// The same for B > 1, followed by the down projection's item lists: ch_list[j] = rc[nC + j] for
+// j < nR, ch_list[nR + j] = rc[S[j]], and the hi / lo bf16 parts of z[b][S[j]] at zk[b][nR + j] /
+// zk_lo[b][nR + j] for j < k, b < B. Launched with programmatic dependent launch.
+cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int nR, int k, int period, int* step,
+                             int* S, const int* rc, int* ch_list, const float* z, int ldz, int B, uint16_t* zk,
+                             uint16_t* zk_lo, int ldk, int N, unsigned* err, cudaStream_t st);
 // sumsq[i] (+)= sum over rows p < rows of part[p * ld + i], p ascending.
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
                               cudaStream_t st);

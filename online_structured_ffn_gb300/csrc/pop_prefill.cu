@@ -328,6 +328,11 @@ bool encode_z_map(CUtensorMap* m, const uint16_t* Z, int M, int N, int ldZ) {
   return encode_2d(m, Z, N, M, static_cast<uint64_t>(ldZ) * 2, BK, BM);
 }
 
+bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int NP) {
+  return encode_2d(m, base, static_cast<uint64_t>(inner), static_cast<uint64_t>(rows), static_cast<uint64_t>(ld) * 2,
+                   64, static_cast<uint32_t>(NP));
+}
+
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_prefill_gateup(const CUtensorMap& x_map, const PrefillMaps& maps, int M, int N, int D,
                                   uint16_t* Z, int ldZ, float* part, int ldPart, unsigned* err, uint64_t wait_ns,

@@ -93,6 +93,54 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   if (threadIdx.x == 0) *step = t + 1;
 }
 
+// ------------------------------------------------------------------ selection for B > 1
+// The top-k of k_select, then the item lists of the down projection. Launched with programmatic
+// dependent launch: nothing of this step is read before griddepcontrol.wait.
+__global__ void __launch_bounds__(SEL_THREADS, 1)
+    k_select_bn(const float* __restrict__ scores, float* __restrict__ memory, int nC, int nR, int k, int period,
+                int* __restrict__ step, int* __restrict__ S, const int* __restrict__ rc, int* __restrict__ ch_list,
+                const float* __restrict__ z, int ldz, int B, uint16_t* __restrict__ zk,
+                uint16_t* __restrict__ zk_lo, int ldk, int N, unsigned* __restrict__ err) {
+  extern __shared__ uint32_t keys[];
+  __shared__ RadixScratch<SEL_THREADS> sc;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int t = *step;
+  bool ok = true;
+  if (nC > 0)
+    ok = select_step<SEL_THREADS>(
+        threadIdx.x, [&](int i) { return scores[i]; }, memory, nC, k, period, (t % period) == 0, keys, S, sc,
+        BlockSync());
+  if (!ok && threadIdx.x == 0) atomicOr(err, DEVERR_TOPK);
+  __syncthreads();
+  if (threadIdx.x == 0) *step = t + 1;
+  for (int j = threadIdx.x; j < nR; j += SEL_THREADS) {
+    const int c = rc[nC + j];
+    if (static_cast<unsigned>(c) >= static_cast<unsigned>(N)) atomicOr(err, DEVERR_INDEX);
+    ch_list[j] = static_cast<unsigned>(c) < static_cast<unsigned>(N) ? c : 0;
+  }
+  // one thread per selected item: its channel, then the hi / lo parts of z for every token (the
+  // token loads are independent, so their latencies overlap)
+  for (int j = threadIdx.x; j < k; j += SEL_THREADS) {
+    int pos = S[j];
+    if (static_cast<unsigned>(pos) >= static_cast<unsigned>(nC)) {
+      atomicOr(err, DEVERR_INDEX);
+      pos = 0;
+    }
+    const int c = rc[pos];
+    if (static_cast<unsigned>(c) >= static_cast<unsigned>(N)) atomicOr(err, DEVERR_INDEX);
+    ch_list[nR + j] = static_cast<unsigned>(c) < static_cast<unsigned>(N) ? c : 0;
+#pragma unroll 8
+    for (int b = 0; b < B; ++b) {
+      const float zz = z[static_cast<size_t>(b) * ldz + pos];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
+      zk[static_cast<size_t>(b) * ldk + nR + j] = *reinterpret_cast<const uint16_t*>(&hi);
+      zk_lo[static_cast<size_t>(b) * ldk + nR + j] = *reinterpret_cast<const uint16_t*>(&lo);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ channel sums of squares
 __global__ void k_fold_sumsq(const float* __restrict__ part, int rows, int ld, int N, float* __restrict__ sumsq,
                              int accumulate) {
@@ -122,6 +170,30 @@ cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int
   }
   k_select<<<1, SEL_THREADS, smem, st>>>(scores, memory, nC, k, period, step, S, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int nR, int k, int period, int* step,
+                             int* S, const int* rc, int* ch_list, const float* z, int ldz, int B, uint16_t* zk,
+                             uint16_t* zk_lo, int ldk, int N, unsigned* err, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(nC > 0 ? nC : 1) * sizeof(uint32_t);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_select_bn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(SEL_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_select_bn, scores, memory, nC, nR, k, period, step, S, rc, ch_list, z, ldz, B,
+                            zk, zk_lo, ldk, N, err);
 }
 
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
