@@ -4,7 +4,7 @@
 // pruning", Fig. 2(a) for the batch max):
 //   gate/up: for every position p of rc = [C | R] and token b, z[b][p] = SiLU(Wg[c] x_b) * (W1[c] x_b)
 //            with c = rc[p]; score[p] = max_b |z[b][p]| * ||W2[:, c]|| for the candidates p < |C|;
-//   down:    y[b][d] = sum over the kept items j of z[b][j] * W2[d, ch_list[j]] (items: R, then S).
+//   down:    y[b][d] = sum over the kept items j (R, then S) of z[b][j] * W2[d, channel of j].
 //
 // The MMA inputs are bf16. x and the weights are bf16 already; z is not, and rounding it to bf16
 // would cost about 3 significant digits of y. So the down GEMM takes z as two bf16 planes, hi =
@@ -14,23 +14,24 @@
 // Both are skinny GEMMs with the tokens as the MMA's N (16..64, zero-padded to a multiple of 16)
 // and 128 rows as M: 128 positions (gate/up; the A tiles are gathered rows of the packed weights,
 // K-major) or 128 outputs d (down; A is gathered down columns, MN-major since d is contiguous in a
-// packed row). The producer warp gathers the rows straight from the packed weights with 16-byte
+// packed row). The producer warps gather the rows straight from the packed weights with 16-byte
 // cp.async copies into the 128-byte swizzle layout (no copy of the pruned weights is ever made;
 // TMA's four-row gather moved too few bytes per operation to keep up with HBM here). The x (or z)
 // tile is an ordinary TMA box.
 //
-// Work split: stream-K over the (tile, 64-wide k-block) iterations, one CTA per SM, so every SM
-// streams the same number of weight bytes (+-1 k-block) whatever the tile count. A CTA's range is a
-// run of segments; a segment that covers a whole tile is finished in place, the others write
-// partial accumulators to a workspace and the last of a tile's contributors (atomic counter) adds
-// them in CTA order (a fixed order: results do not depend on timing) and finishes the tile.
+// Work split. With few tiles (the usual decode shapes: |R u C| / 128 or D / 128 is well below the
+// SM count) every tile is split along K over a cluster of `split` CTAs (1 CTA per SM, 2 / 4 / 8 per
+// cluster); each CTA streams 1/split of the tile's k-blocks, then the partial accumulators are
+// added through distributed shared memory in rank order (a fixed order: results do not depend on
+// timing), each CTA finishing 128 / split of the rows. No workspace, no atomics. With many tiles
+// (split = 1), CTAs take whole tiles round-robin and finish them straight from TMEM.
 //
-// Roles (192 threads): warp 0 issues the copies, warp 1 lane 0
-// issues the MMAs and owns TMEM (two accumulator buffers, so the epilogue of one segment overlaps
-// the MMAs of the next), warps 2..5 are the epilogue (one TMEM lane quarter each). Every wait is
-// bounded; on a time-out the CTA records DEVERR_TIMEOUT_DECODE_TC, stops issuing, drains its own
-// copies and MMAs (bounded), frees TMEM and returns. The epilogue warps take every decision that
-// guards a named barrier together, so a time-out cannot leave one of them waiting at a barrier.
+// Roles (224 threads): warps 0-1 issue the copies, warp 2 lane 0 issues the MMAs and owns TMEM
+// (two accumulator buffers, so the epilogue of one tile overlaps the MMAs of the next), warps 3-6
+// are the epilogue (one TMEM lane quarter each). Every wait is bounded; on a time-out the CTA
+// records DEVERR_TIMEOUT_DECODE_TC, stops issuing, drains its own copies and MMAs (bounded), frees
+// TMEM and returns. The epilogue warps take every decision that guards a named barrier together,
+// and every thread reaches the cluster barriers, so a time-out cannot leave a barrier waiting.
 //
 // Programmatic dependent launch: the set-up (barriers, TMEM, tensor-map prefetch) runs before
 // griddepcontrol.wait; every global read or write of this step's data comes after it.
@@ -40,27 +41,31 @@
 namespace pop {
 
 namespace {
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 224;
+constexpr int TC_PRODUCERS = 2;  // warps 0-1 gather rows, warp 2 issues MMAs, warps 3-6 are the epilogue
+constexpr int TC_MMA_WARP = TC_PRODUCERS;
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 constexpr uint64_t TC_DRAIN_NS = 1000000000ull;
-constexpr int TC_WS_COLS = 128;  // workspace columns per slot (2 x 64 tokens for gate/up)
+// shared memory for the stage ring (the down kernel also keeps its row-offset windows)
+constexpr uint32_t TC_RING_BUDGET[2] = {210 * 1024, 192 * 1024};
+// down: row offsets of the items of up to TC_WIN k-blocks, per producer warp (its 32 rows of each)
+constexpr int TC_WIN = 64;
 
-template <int MODE>
-struct TcCfg;
-template <>
-struct TcCfg<0> {  // gate/up: A = 128 gate rows + 128 up rows, B = x
-  static constexpr int STAGES = 5;
-  static constexpr uint32_t A_BYTES = 2 * TC_BM * TC_BK * 2;  // 32 KB
-  static constexpr uint32_t B_BYTES = 64 * TC_BK * 2;         // room for 64 tokens
-  static constexpr uint32_t TMEM_COLS = 256;                  // two buffers of [g | u] x 64 tokens
-};
-template <>
-struct TcCfg<1> {  // down: A = 64 items x 128 outputs (two 64-wide halves), B = z hi and lo planes
-  static constexpr int STAGES = 6;
-  static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
-  static constexpr uint32_t B_BYTES = 2 * 64 * TC_BK * 2;  // room for 2 x 64 token rows
-  static constexpr uint32_t TMEM_COLS = 256;               // two buffers of [hi | lo] x 64 tokens
+// Stage layout: A (weight rows) then B (token tile). Gate/up: A = 128 gate rows + 128 up rows of
+// 128 bytes, B = NP rows of x. Down: A = 64 items x 128 outputs (two 64-wide halves), B = the hi
+// and lo planes of z, NP rows each. As many stages as fit the budget (at most 8).
+template <int MODE, int NP>
+struct TcCfg {
+  static constexpr uint32_t A_BYTES = MODE == 0 ? 2 * TC_BM * TC_BK * 2 : TC_BM * TC_BK * 2;
+  static constexpr uint32_t B_BYTES = (MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = TC_RING_BUDGET[MODE] / STAGE_BYTES < 8 ? TC_RING_BUDGET[MODE] / STAGE_BYTES : 8;
+  static constexpr uint32_t TMEM_COLS = 256;  // two accumulator buffers of 2 x NP <= 128 columns
+  // partial accumulators exchanged in a cluster, fp32 per row: [g | u] (gate/up) or hi + lo (down)
+  static constexpr int PCOLS = MODE == 0 ? 2 * NP : NP;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  static_assert(static_cast<uint32_t>(TC_BM * PCOLS * 4) <= STAGES * STAGE_BYTES, "partials reuse the ring");
 };
 
 struct TcCtl {
@@ -71,13 +76,14 @@ struct TcCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int seg_ok[2];  // by segment parity: a warp may still read one while the next is written
-  int last;
+  int seg_ok[2];  // by tile parity: a warp may still read one while the next is written
+  float n2s[TC_BM];                 // gate/up, split tiles: norms of the rows each epilogue thread finishes
 };
 
-template <int MODE>
+template <int MODE, int NP>
 constexpr size_t tc_smem_bytes() {
-  return 1024 + TcCfg<MODE>::STAGES * (TcCfg<MODE>::A_BYTES + TcCfg<MODE>::B_BYTES) + sizeof(TcCtl);
+  return 1024 + TcCfg<MODE, NP>::STAGES * TcCfg<MODE, NP>::STAGE_BYTES + sizeof(TcCtl) +
+         (MODE == 1 ? TC_PRODUCERS * TC_WIN * 32 * sizeof(uint32_t) : 0);
 }
 
 __device__ __forceinline__ float silu_t(float g) { return g / (1.0f + expf(-g)); }
@@ -107,17 +113,26 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel_tc(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+// All threads of all CTAs of the cluster; orders shared-memory writes before the barrier with
+// (distributed) shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-
-// Stream-K partition of T iterations over G CTAs: CTA c owns [start(c), start(c + 1)).
-__device__ __forceinline__ long long sk_start(int c, long long T, int G) { return static_cast<long long>(c) * T / G; }
-// The CTA that owns iteration i.
-__device__ __forceinline__ int sk_owner(long long i, long long T, int G) {
-  return static_cast<int>(((i + 1) * G - 1) / T);
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_peer2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 }  // namespace
 
@@ -127,9 +142,9 @@ template <int MODE, int NP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_decode_tc(const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapB2,
                 const __grid_constant__ DecodeTcArgs a) {
-  using Cfg = TcCfg<MODE>;
+  using Cfg = TcCfg<MODE, NP>;
   constexpr int STAGES = Cfg::STAGES;
-  constexpr uint32_t STAGE_BYTES = Cfg::A_BYTES + Cfg::B_BYTES;
+  constexpr uint32_t STAGE_BYTES = Cfg::STAGE_BYTES;
   constexpr uint32_t HALF_COLS = Cfg::TMEM_COLS / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,16 +153,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (a.rows + TC_BM - 1) / TC_BM;
   const int KB = (a.K + TC_BK - 1) / TC_BK;
-  const long long T = static_cast<long long>(tiles) * KB;
-  const int G = gridDim.x;
-  const long long s_begin = sk_start(blockIdx.x, T, G), s_end = sk_start(blockIdx.x + 1, T, G);
+  // this CTA's work: tiles unit, unit + nunits, ...; k-blocks [kb_lo, kb_hi) of each
+  const int SK = a.split;
+  const uint32_t rank = SK > 1 ? cluster_rank() : 0u;
+  const int unit = static_cast<int>(blockIdx.x) / SK, nunits = static_cast<int>(gridDim.x) / SK;
+  const int kb_lo = static_cast<int>(rank) * KB / SK, kb_hi = (static_cast<int>(rank) + 1) * KB / SK;
   // bytes the TMA boxes bring per stage (the weight rows come by cp.async): NP token rows of x
   // (gate/up) or 2 x NP (the hi and lo planes of z, down)
   const uint32_t tx_bytes = static_cast<uint32_t>(MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctl->full[s], 33);  // the producer's 32 lanes + lane 0's TMA transaction count
+      mbar_init(&ctl->full[s], 32 * TC_PRODUCERS + 1);  // producer lanes + the TMA transaction count
       mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -160,7 +177,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (MODE == 1) prefetch_tmap(&mapB2);
     prefetch_tmap(&mapB);
   }
-  if (warp == 1) {
+  if (warp == TC_MMA_WARP) {
     tmem_alloc(&ctl->tmem_base, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
@@ -178,39 +195,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer (whole warp)
-    // The weight rows of a stage are gathered with 16-byte cp.async copies (lane l copies chunk
-    // l % 8 of rows l / 8, l / 8 + 4, ...), each written to its place in the 128-byte swizzle
-    // pattern; the token tile (x, or the two z planes) is a TMA box. One commit group per stage:
-    // once a lane's group for stage i has landed (checked LAG stages later, so LAG + 1 stages of
-    // copies stay in flight) the lane fences its writes for the async proxy and arrives on the
-    // stage's barrier; lane 0 also arrives with the TMA byte count when it issues the box.
-    const int cq = lane & 7, rg = lane >> 3;
-    constexpr int LAG = STAGES - 2;
+  if (warp < TC_PRODUCERS) {
+    // ------------------------------------------------------------ producers (two whole warps)
+    // The weight rows of a stage are gathered with 16-byte cp.async copies (lane l of producer warp
+    // w copies chunk l % 8 of rows rg, rg + 8, ... with rg = l / 8 + 4 w), each written to its place
+    // in the 128-byte swizzle pattern; the token tile (x, or the two z planes) is a TMA box issued
+    // by warp 0. One commit group per stage: once a lane's group for stage i has landed (checked LAG
+    // stages later, so LAG + 1 stages of copies stay in flight) the lane fences its writes for the
+    // async proxy and arrives on the stage's barrier; warp 0 lane 0 also arrives with the TMA byte
+    // count when it issues the box.
+    const int cq = lane & 7, rg = (lane >> 3) + 4 * warp;
+    constexpr int LAG = STAGES - 1;
     const uint16_t* Wbase = a.Wp + (MODE == 0 ? 0 : 2 * static_cast<size_t>(a.D));
     const size_t row3 = 3 * static_cast<size_t>(a.D);
     uint32_t issued = 0;
     bool ok = true;
-    for (long long i = s_begin; i < s_end && ok;) {
-      const int tile = static_cast<int>(i / KB);
-      const int kb0 = static_cast<int>(i - static_cast<long long>(tile) * KB);
-      const long long e = min(s_end, static_cast<long long>(tile + 1) * KB);
-      const int kb1 = kb0 + static_cast<int>(e - i);
-      // MODE 0: the tile's 128 rows are positions 128 * tile + r (fixed over the segment); this lane
-      // copies rows rg + 4m. MODE 1: the k-block's 64 rows are items 64 * kb + r; this lane copies
-      // items rg + 4m, and the next k-block's ids are loaded before this one's wait so that their
-      // latency hides behind it. Row offsets (elements) stay in registers.
-      constexpr int NROW = MODE == 0 ? TC_BM / 4 : TC_BK / 4;
-      uint32_t rowoff[NROW];
-      int ids_nxt[NROW];
-      auto load_ids = [&](int kb, int (&o)[NROW]) {
+    // Down: the row offsets of the items this warp copies (rows rg + 8m of each k-block), for a
+    // window of up to TC_WIN k-blocks at a time, in shared memory. Lane l of warp w fetches item
+    // (4w + l % 4) + 8 (l / 4) of each k-block of the window (one load per k-block, all in flight at
+    // once); the lane that copies rows rg + 8m reads entry (rg - 4w) + 4m. Each warp fills and reads
+    // only its own table, so the warps never wait on each other.
+    uint32_t* win = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(TcCtl)) +
+                    warp * TC_WIN * 32;
+    int win_lo = -1, win_hi = -1;  // k-blocks [win_lo, win_hi) are in the window
+    auto fill_window = [&](int kb0w) {
+      win_lo = kb0w;
+      win_hi = min(kb_hi, kb0w + TC_WIN);
+      const int item_in_kb = 4 * warp + (lane & 3) + 8 * (lane >> 2);
+      __syncwarp();
+      for (int c0 = win_lo; c0 < win_hi; c0 += 16) {
+        int v[16];
 #pragma unroll
-        for (int m = 0; m < NROW; ++m) {
-          const int item = kb * TC_BK + rg + 4 * m;
-          o[m] = item < a.K ? a.ch_list[item] : 0;
+        for (int u = 0; u < 16; ++u) {
+          const int item = (c0 + u) * TC_BK + item_in_kb;
+          v[u] = 0;
+          if (c0 + u < win_hi && item < a.K) v[u] = item < a.nR_items ? a.ch_r[item] : a.ch_s[item - a.nR_items];
         }
-      };
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (c0 + u < win_hi) win[(c0 + u - win_lo) * 32 + lane] = static_cast<uint32_t>(guard_ch(v[u], a.N, a.err)) * row3;
+      }
+      __syncwarp();
+    };
+    for (int tile = unit; tile < tiles && ok; tile += nunits) {
+      // MODE 0: the tile's 128 rows are positions 128 * tile + r; this lane copies rows rg + 8m.
+      // MODE 1: the k-block's 64 rows are items 64 * kb + r; this lane copies items rg + 8m.
+      // Row offsets (elements) stay in registers.
+      constexpr int NROW = MODE == 0 ? TC_BM / 8 : TC_BK / 8;
+      uint32_t rowoff[NROW];
       auto set_rows = [&](const int (&ids)[NROW]) {
 #pragma unroll
         for (int m = 0; m < NROW; ++m) rowoff[m] = static_cast<uint32_t>(guard_ch(ids[m], a.N, a.err)) * row3;
@@ -219,17 +251,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int ids[NROW];
 #pragma unroll
         for (int m = 0; m < NROW; ++m) {
-          const int p = tile * TC_BM + rg + 4 * m;
+          const int p = tile * TC_BM + rg + 8 * m;
           ids[m] = p < a.rows ? a.rc[p] : 0;
         }
         set_rows(ids);
-      } else {
-        load_ids(kb0, ids_nxt);
       }
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (MODE == 1) {
-          set_rows(ids_nxt);
-          if (kb + 1 < kb1) load_ids(kb + 1, ids_nxt);
+          if (kb < win_lo || kb >= win_hi) fill_window(kb);
+          const uint32_t* wrow = win + (kb - win_lo) * 32 + (rg - 4 * warp);
+#pragma unroll
+          for (int m = 0; m < NROW; ++m) rowoff[m] = wrow[4 * m];
         }
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1u;
@@ -237,7 +269,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
           got = mbar_wait_bounded(&ctl->empty[s], ph ^ 1u, a.wait_ns, abort_flag);
           if (!got) fail();
-          else mbar_arrive_expect_tx(&ctl->full[s], tx_bytes);
+          else if (warp == 0) mbar_arrive_expect_tx(&ctl->full[s], tx_bytes);
         }
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
@@ -252,7 +284,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint16_t* base = Wbase + (nbytes ? d0 : 0);
 #pragma unroll
           for (int m = 0; m < NROW; ++m) {
-            const int r = rg + 4 * m;
+            const int r = rg + 8 * m;
             const uint32_t dst = sa + r * 128 + ((cq ^ (r & 7)) << 4);
             cp_async16(dst, base + rowoff[m], nbytes);
             cp_async16(dst + TC_BM * 128, base + rowoff[m] + a.D, nbytes);
@@ -265,7 +297,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint16_t* base = Wbase + (nbytes ? d0 : 0);
 #pragma unroll
             for (int m = 0; m < NROW; ++m) {
-              const int r = rg + 4 * m;
+              const int r = rg + 8 * m;
               cp_async16(sa + h * (TC_BK * 128) + r * 128 + ((cq ^ (r & 7)) << 4), base + rowoff[m], nbytes);
             }
           }
@@ -276,13 +308,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           fence_proxy_async();
           mbar_arrive(&ctl->full[(issued - LAG) % STAGES]);
         }
-        if (lane == 0) {
+        if (warp == 0 && lane == 0) {
           tma_load_2d(sb, &mapB, &ctl->full[s], kb * TC_BK, 0);
           if (MODE == 1) tma_load_2d(sb + NP * 128, &mapB2, &ctl->full[s], kb * TC_BK, 0);  // z lo plane
         }
         ++issued;
       }
-      i = e;
     }
     // the last stages' arrivals, and every copy this warp started must land before the CTA can exit
     cp_async_wait<0>();
@@ -290,7 +321,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (ok)
       for (uint32_t u = issued > static_cast<uint32_t>(LAG) ? issued - LAG : 0; u < issued; ++u)
         mbar_arrive(&ctl->full[u % STAGES]);
-    if (lane == 0) {
+    if (warp == 0 && lane == 0) {
       const uint32_t lo = issued > static_cast<uint32_t>(STAGES) ? issued - STAGES : 0;
       for (uint32_t u = lo; u < issued; ++u) {
         volatile int never = 0;
@@ -298,18 +329,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == TC_MMA_WARP) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
       const uint32_t idesc = idesc_bf16_f32(TC_BM, MODE == 0 ? NP : 2 * NP, false, MODE == 1);
       uint32_t consumed = 0;
       int it = 0;
       bool ok = true;
-      for (long long i = s_begin; i < s_end && ok; ++it) {
-        const int tile = static_cast<int>(i / KB);
-        const int kb0 = static_cast<int>(i - static_cast<long long>(tile) * KB);
-        const long long e = min(s_end, static_cast<long long>(tile + 1) * KB);
-        const int kb1 = kb0 + static_cast<int>(e - i);
+      for (int tile = unit; tile < tiles && ok; tile += nunits, ++it) {
         const int buf = it & 1;
         if (!mbar_wait_bounded(&ctl->tempty[buf], ((it >> 1) & 1) ^ 1, a.wait_ns, abort_flag)) {
           fail();
@@ -317,7 +344,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * HALF_COLS;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           const int s = consumed % STAGES;
           const uint32_t ph = (consumed / STAGES) & 1u;
           if (!mbar_wait_bounded(&ctl->full[s], ph, a.wait_ns, abort_flag)) {
@@ -330,7 +357,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
           for (int k = 0; k < TC_BK / 16; ++k) {
-            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > kb_lo || k > 0) ? 1u : 0u;
             const uint64_t bdesc = smem_desc_sw128(sb + 32u * k, 16u, 1024u);
             if (MODE == 0) {
               umma_f16(d_tmem, smem_desc_sw128(sa + 32u * k, 16u, 1024u), bdesc, idesc, acc);
@@ -345,7 +372,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (!ok) break;
         umma_commit(&ctl->tfull[buf]);
-        i = e;
       }
       // all MMAs issued by this thread must finish before TMEM is freed
       umma_commit(&ctl->drain);
@@ -354,17 +380,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 3..6)
     const int q = warp & 3;  // TMEM lane quarter of this warp
     const int r = 32 * q + lane;
-    const int et = threadIdx.x - 64;  // 0..127
-    int it = 0, seg = 0;
-    for (long long i = s_begin; i < s_end; ++it, ++seg) {
-      const int tile = static_cast<int>(i / KB);
-      const int kb0 = static_cast<int>(i - static_cast<long long>(tile) * KB);
-      const long long e = min(s_end, static_cast<long long>(tile + 1) * KB);
-      const int kb1 = kb0 + static_cast<int>(e - i);
+    const int et = threadIdx.x - 32 * (TC_MMA_WARP + 1);  // 0..127
+    // split tiles: the norm of the candidate row this thread finishes after the cluster exchange,
+    // fetched now while the tile streams
+    if (MODE == 0 && SK > 1 && unit < tiles) {
+      const int p = unit * TC_BM + static_cast<int>(rank) * (TC_BM / SK) + et / SK;
+      if (p < a.nC) ctl->n2s[et] = a.n2[guard_ch(a.rc[p], a.N, a.err)];
+    }
+    int it = 0;
+    for (int tile = unit; tile < tiles; tile += nunits, ++it) {
       const int buf = it & 1;
+      // the candidates' down-column norms, fetched while the accumulators are still being built
+      float n2v = 0.f;
+      if (MODE == 0 && SK == 1) {
+        const int p = tile * TC_BM + r;
+        if (p < a.nC) n2v = a.n2[guard_ch(a.rc[p], a.N, a.err)];
+      }
       if (et == 0)
         ctl->seg_ok[it & 1] = mbar_wait_bounded(&ctl->tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
       epi_bar();
@@ -392,98 +426,143 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
 
-      bool finish = kb0 == 0 && kb1 == KB;
-      if (!finish) {
-        // partial tile: publish, then the last contributor adds all partials in CTA order
-        const int slot = 2 * blockIdx.x + (seg == 0 ? 0 : 1);
-        float* w = a.ws + static_cast<size_t>(slot) * TC_WS_COLS * TC_BM;
+      if (SK > 1) {
+        // partial of a split tile: to this CTA's shared memory (the stage ring, idle by now: all
+        // copies landed and all MMAs finished), rows of PCOLS floats
+        float* pb = reinterpret_cast<float*>(smem) + r * Cfg::PCOLS;
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
-          w[c * TC_BM + r] = gv[c];
-          w[(NP + c) * TC_BM + r] = uv[c];
-        }
-        epi_bar();
-        if (et == 0) {
-          const long long t0 = static_cast<long long>(tile) * KB;
-          const int c_lo = sk_owner(t0, T, G), c_hi = sk_owner(t0 + KB - 1, T, G);
-          unsigned* cnt = a.tile_cnt + tile;
-          const unsigned old = atom_add_acq_rel_tc(cnt, 1u);
-          const int last = old + 1 == static_cast<unsigned>(c_hi - c_lo + 1);
-          if (last) atomicExch(cnt, 0u);  // every contributor has arrived: ready for the next launch
-          ctl->last = last;
-        }
-        epi_bar();
-        finish = ctl->last != 0;
-        if (finish) {
-          const long long t0 = static_cast<long long>(tile) * KB;
-          const int c_lo = sk_owner(t0, T, G), c_hi = sk_owner(t0 + KB - 1, T, G);
-#pragma unroll
-          for (int c = 0; c < NP; ++c) {
-            gv[c] = 0.f;
-            uv[c] = 0.f;
+          if (MODE == 0) {
+            pb[c] = gv[c];
+            pb[NP + c] = uv[c];
+          } else {
+            pb[c] = gv[c] + uv[c];
           }
-          for (int cc = c_lo; cc <= c_hi; ++cc) {
-            const int sl = 2 * cc + (sk_start(cc, T, G) >= t0 ? 0 : 1);
-            const float* wp = a.ws + static_cast<size_t>(sl) * TC_WS_COLS * TC_BM + r;
-            float lg[NP], lu[NP];
+        }
+        continue;
+      }
+      if (MODE == 0) {
+        const int p = tile * TC_BM + r;
+        if (p < a.rows) {
+          float m = 0.f;
 #pragma unroll
-            for (int c = 0; c < NP; ++c) {
-              lg[c] = __ldcg(wp + c * TC_BM);
-              lu[c] = __ldcg(wp + (NP + c) * TC_BM);
+          for (int b = 0; b < NP; ++b) {
+            if (b < a.B) {
+              const float zz = silu_t(gv[b]) * uv[b];
+              a.z[static_cast<size_t>(b) * a.ldz + p] = zz;
+              if (p >= a.nC) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
+                const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
+                a.zk[o] = *reinterpret_cast<const uint16_t*>(&hi);
+                a.zk_lo[o] = *reinterpret_cast<const uint16_t*>(&lo);
+              }
+              m = fmaxf(m, fabsf(zz));
             }
+          }
+          if (p < a.nC) a.scores[p] = m * n2v;
+        }
+      } else {
+        const int d = tile * TC_BM + r;
+        if (d < a.rows) {
 #pragma unroll
-            for (int c = 0; c < NP; ++c) {
-              gv[c] += lg[c];
-              uv[c] += lu[c];
+          for (int b = 0; b < NP; ++b) {
+            if (b < a.B) {
+              const float yv = gv[b] + uv[b];
+              if (a.out_f32)
+                static_cast<float*>(a.y)[static_cast<size_t>(b) * a.rows + d] = yv;
+              else
+                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.rows + d] = __float2bfloat16_rn(yv);
             }
           }
         }
       }
-      if (finish) {
-        if (MODE == 0) {
-          const int p = tile * TC_BM + r;
-          if (p < a.rows) {
-            float m = 0.f;
+    }
+  }
+
+  if (SK > 1) {
+    // ------------------------------------------------------------ cluster reduction of the split tile
+    // Every thread of the cluster passes both barriers. Between them, epilogue thread et of rank
+    // `rank` finishes row rank * 128 / SK + et / SK for tokens [part * NP / SK, (part + 1) * NP / SK),
+    // part = et % SK, adding the SK partials in rank order.
+    cluster_sync_all();
+    if (warp > TC_MMA_WARP && unit < tiles && !*abort_flag) {
+      const int et = threadIdx.x - 32 * (TC_MMA_WARP + 1);
+      const int rows_per = TC_BM / SK, tpt = NP / SK;
+      const int rl = et / SK, part = et % SK;
+      const int row = static_cast<int>(rank) * rows_per + rl;
+      const int b0 = part * tpt;
+      const uint32_t pbase = smem_u32(smem) + static_cast<uint32_t>(row * Cfg::PCOLS) * 4u;
+      float m = 0.f;
+      const int p = unit * TC_BM + row;
+      const float n2v = MODE == 0 && p < a.nC ? ctl->n2s[et] : 0.f;
+      uint32_t peer[8];
 #pragma unroll
-            for (int b = 0; b < NP; ++b) {
-              if (b < a.B) {
-                const float zz = silu_t(gv[b]) * uv[b];
-                a.z[static_cast<size_t>(b) * a.ldz + p] = zz;
-                if (p >= a.nC) {
-                  const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
-                  const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
-                  const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
-                  a.zk[o] = *reinterpret_cast<const uint16_t*>(&hi);
-                  a.zk_lo[o] = *reinterpret_cast<const uint16_t*>(&lo);
-                }
-                m = fmaxf(m, fabsf(zz));
-              }
+      for (int pr = 0; pr < 8; ++pr) peer[pr] = pr < SK ? map_peer(pbase, static_cast<uint32_t>(pr)) : 0u;
+      // tokens two at a time (tpt = NP / SK is even): SK peers x 8-byte loads, added in rank order
+#pragma unroll 2
+      for (int j = 0; j < tpt; j += 2) {
+        const int b = b0 + j;
+        float2 g2 = make_float2(0.f, 0.f), u2 = make_float2(0.f, 0.f);
+        float2 lg[8], lu[8];
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) {
+          if (pr < SK) {
+            lg[pr] = ld_peer2(peer[pr] + 4u * b);
+            if (MODE == 0) lu[pr] = ld_peer2(peer[pr] + 4u * (NP + b));
+          }
+        }
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) {
+          if (pr < SK) {
+            g2.x += lg[pr].x;
+            g2.y += lg[pr].y;
+            if (MODE == 0) {
+              u2.x += lu[pr].x;
+              u2.y += lu[pr].y;
             }
-            if (p < a.nC) a.scores[p] = m * a.n2[guard_ch(a.rc[p], a.N, a.err)];
+          }
+        }
+        for (int h = 0; h < 2; ++h) {
+        const int b = b0 + j + h;
+        const float g = h ? g2.y : g2.x, u = h ? u2.y : u2.x;
+        if (b >= a.B) continue;
+        if (MODE == 0) {
+          if (p < a.rows) {
+            const float zz = silu_t(g) * u;
+            a.z[static_cast<size_t>(b) * a.ldz + p] = zz;
+            if (p >= a.nC) {
+              const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
+              const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
+              const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
+              a.zk[o] = *reinterpret_cast<const uint16_t*>(&hi);
+              a.zk_lo[o] = *reinterpret_cast<const uint16_t*>(&lo);
+            }
+            m = fmaxf(m, fabsf(zz));
           }
         } else {
-          const int d = tile * TC_BM + r;
+          const int d = unit * TC_BM + row;
           if (d < a.rows) {
-#pragma unroll
-            for (int b = 0; b < NP; ++b) {
-              if (b < a.B) {
-                const float yv = gv[b] + uv[b];
-                if (a.out_f32)
-                  static_cast<float*>(a.y)[static_cast<size_t>(b) * a.rows + d] = yv;
-                else
-                  static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.rows + d] = __float2bfloat16_rn(yv);
-              }
-            }
+            if (a.out_f32)
+              static_cast<float*>(a.y)[static_cast<size_t>(b) * a.rows + d] = g;
+            else
+              static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.rows + d] = __float2bfloat16_rn(g);
           }
         }
+        }
       }
-      i = e;
+      if (MODE == 0) {
+        // the row's SK threads are adjacent lanes: combine their maxima
+        for (int o = SK / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (part == 0 && p < a.nC) a.scores[p] = m * n2v;
+      }
     }
+    cluster_sync_all();  // no CTA leaves while a peer may still read its partials
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == TC_MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
@@ -491,9 +570,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ------------------------------------------------------------------ launchers
 template <int MODE, int NP>
-static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, const DecodeTcArgs& args, int grid,
+static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, DecodeTcArgs args, int num_sms,
                                 cudaStream_t st) {
-  constexpr size_t smem = tc_smem_bytes<MODE>();
+  constexpr size_t smem = tc_smem_bytes<MODE, NP>();
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k_decode_tc<MODE, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -501,30 +580,49 @@ static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, con
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  const int tiles = (args.rows + TC_BM - 1) / TC_BM;
+  const int KB = (args.K + TC_BK - 1) / TC_BK;
+  if (tiles <= 0 || KB <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // split: the largest power of two <= 8 such that tiles x split CTAs fit the SMs at once (one CTA
+  // per SM) with at least one k-block per CTA, confirmed by the cluster occupancy query
+  int split = 1;
+  while (split < 8 && tiles * split * 2 <= num_sms && split * 2 <= KB) split *= 2;
+  for (; split > 1; split /= 2) {
+    attr[1].val.clusterDim.x = split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(tiles * split);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k_decode_tc<MODE, NP>, &cfg) == cudaSuccess && clusters >= tiles)
+      break;
+    (void)cudaGetLastError();
+  }
+  args.split = split;
+  if (split == 1) {
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
+  }
   return cudaLaunchKernelEx(&cfg, k_decode_tc<MODE, NP>, b, b2, args);
 }
 
 template <int MODE>
 static cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& b2, const DecodeTcArgs& args, int num_sms,
                              cudaStream_t st) {
-  const long long T = static_cast<long long>((args.rows + TC_BM - 1) / TC_BM) * ((args.K + TC_BK - 1) / TC_BK);
-  if (T <= 0) return cudaSuccess;
-  const int grid = static_cast<int>(T < num_sms ? T : num_sms);
   switch (args.NP) {
-    case 16: return launch_tc_np<MODE, 16>(b, b2, args, grid, st);
-    case 32: return launch_tc_np<MODE, 32>(b, b2, args, grid, st);
-    case 48: return launch_tc_np<MODE, 48>(b, b2, args, grid, st);
-    case 64: return launch_tc_np<MODE, 64>(b, b2, args, grid, st);
+    case 16: return launch_tc_np<MODE, 16>(b, b2, args, num_sms, st);
+    case 32: return launch_tc_np<MODE, 32>(b, b2, args, num_sms, st);
+    case 48: return launch_tc_np<MODE, 48>(b, b2, args, num_sms, st);
+    case 64: return launch_tc_np<MODE, 64>(b, b2, args, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -537,7 +635,5 @@ cudaError_t launch_down_tc(const CUtensorMap& zk_map, const CUtensorMap& zk_lo_m
                            int num_sms, cudaStream_t st) {
   return launch_tc<1>(zk_map, zk_lo_map, args, num_sms, st);
 }
-
-size_t decode_tc_workspace_floats(int num_sms) { return static_cast<size_t>(2) * num_sms * TC_WS_COLS * TC_BM; }
 
 }  // namespace pop

@@ -42,9 +42,7 @@ struct pop_ffn {
   // B > 1 decode (tensor-core kernels)
   uint16_t* zk = nullptr;  // [2][max_batch][ldk]: bf16 hi and lo parts of z of the kept items (R, then S)
   int ldk = 0;
-  int* ch_list = nullptr;  // kept item -> channel
-  float* ws = nullptr;     // stream-K partial accumulators
-  unsigned* tc_cnt = nullptr;  // per-tile counters: [0, kTcDownCnt) gate/up, [kTcDownCnt, ..) down
+  int* ch_s = nullptr;     // channels of the selected candidates, in S order
   int* step = nullptr;
   unsigned* err = nullptr;
   unsigned* fsync = nullptr;  // inter-CTA counters of the decode kernels
@@ -64,9 +62,6 @@ static constexpr int kProfEvents = 5;
 // device counters: [4] candidates scored by the B = 1 gate/up, [8..] tiles of y done by the down chunks
 static constexpr int kSyncWords = 64;
 static constexpr int kProfMaxSteps = 256;
-// stream-K tile counters of the B > 1 kernels: gate/up tiles (<= D_FF / 128) first, then down tiles (<= D / 128)
-static constexpr int kTcDownCnt = (POP_MAX_D_FF + 127) / 128;
-static constexpr int kTcCntWords = kTcDownCnt + (POP_MAX_D + 127) / 128;
 
 namespace {
 thread_local std::string g_msg;
@@ -123,8 +118,8 @@ void prof_end(pop_ffn* h) {
 
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
-                  h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_list,
-                  h->ws,    h->tc_cnt, h->step, h->err,     h->fsync};
+                  h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_s,
+                  h->step, h->err,     h->fsync};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -158,9 +153,7 @@ DecodeB1Args b1_args(pop_ffn* h, const uint16_t* x, void* y, const int* rc, int 
 // Zeroes every inter-CTA counter of the decode kernels (they are left at zero by each launch that
 // completes, so this only matters after a partition change or a reported device error).
 cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
-  if (e == cudaSuccess && h->tc_cnt) e = cudaMemsetAsync(h->tc_cnt, 0, kTcCntWords * sizeof(unsigned), st);
-  return e;
+  return cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
 }
 
 // gate/up over positions [0, nRC) of rc for B tokens: z, zk (positions >= nC) and scores (< nC).
@@ -182,8 +175,6 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nR
   a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
   a.ldk = h->ldk;
   a.scores = h->scores;
-  a.ws = h->ws;
-  a.tile_cnt = h->tc_cnt;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   CUtensorMap xm;
@@ -193,8 +184,10 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nR
   return POP_OK;
 }
 
-// y[b] = sum over the nK kept items j of zk[b][j] * W2[:, ch_list[j]] for B tokens.
-pop_status down_tc(pop_ffn* h, int B, const int* ch_list, int nK, void* y, cudaStream_t st) {
+// y[b] = sum over the kept items j of z[b][j] W2[:, channel of j] for B tokens: the nR items with
+// channels ch_r[], then the k items with channels ch_s[].
+pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, const int* ch_s, int k, void* y, cudaStream_t st) {
+  const int nK = nR + k;
   if (nK <= 0) {
     const size_t bytes = static_cast<size_t>(B) * h->D * (h->cfg.out_f32 ? 4 : 2);
     POP_CUDA(h, cudaMemsetAsync(y, 0, bytes, st));
@@ -208,11 +201,11 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_list, int nK, void* y, cudaS
   a.rows = h->D;
   a.K = nK;
   a.N = h->N;
-  a.ch_list = ch_list;
+  a.ch_r = ch_r;
+  a.ch_s = ch_s;
+  a.nR_items = nR;
   a.y = y;
   a.out_f32 = h->cfg.out_f32;
-  a.ws = h->ws;
-  a.tile_cnt = h->tc_cnt + kTcDownCnt;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   CUtensorMap zm, zlm;
@@ -339,9 +332,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
   if (cfg->max_batch > 1) {
     POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
-    POP_ALLOC(h->ch_list, N);
-    POP_ALLOC(h->ws, decode_tc_workspace_floats(h->num_sms));
-    POP_ALLOC(h->tc_cnt, kTcCntWords);
+    POP_ALLOC(h->ch_s, N);
   }
   POP_ALLOC(h->step, 1);
   POP_ALLOC(h->err, 1);
@@ -350,9 +341,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   if ((e = cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st)) != cudaSuccess)
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
-  if (h->tc_cnt && (e = cudaMemsetAsync(h->tc_cnt, 0, kTcCntWords * sizeof(unsigned), st)) != cudaSuccess)
-    return bail(e, "cudaMemsetAsync");
-  if (h->ch_list && (e = cudaMemsetAsync(h->ch_list, 0, sizeof(int) * N, st)) != cudaSuccess)
+  if (h->ch_s && (e = cudaMemsetAsync(h->ch_s, 0, sizeof(int) * N, st)) != cudaSuccess)
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection
@@ -500,18 +489,17 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     prof_mark(h, 3, st);
     prof_mark(h, 4, st);
   } else {
-    const int nK = nR + h->cnt.k;
     prof_mark(h, 0, st);
     if (nRC > 0) {
       pop_status s = gateup_tc(h, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, st);
       if (s != POP_OK) return s;
     }
     prof_mark(h, 1, st);
-    POP_CUDA(h, launch_select_bn(h->scores, h->memory, nC, nR, h->cnt.k, h->cfg.period, h->step, h->S, h->rc,
-                                 h->ch_list, h->z, nRC, B, h->zk,
-                                 h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, h->ldk, h->N, h->err, st));
+    POP_CUDA(h, launch_select_bn(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+    POP_CUDA(h, launch_pack_selected(h->S, h->cnt.k, nC, h->rc, h->N, h->ch_s, h->z, nRC, B, h->zk,
+                                     h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, h->ldk, nR, h->err, st));
     prof_mark(h, 2, st);
-    pop_status s = down_tc(h, B, h->ch_list, nK, y, st);
+    pop_status s = down_tc(h, B, h->rc + nC, nR, h->ch_s, h->cnt.k, y, st);
     if (s != POP_OK) return s;
     prof_mark(h, 3, st);
     prof_mark(h, 4, st);
@@ -537,7 +525,7 @@ pop_status pop_ffn_dense_ref(pop_ffn_t h, const void* X, int M, void* Y, void* s
   // 2 <= M <= max_batch: the decode kernels over every channel (all positions count as retained)
   pop_status s = gateup_tc(h, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, st);
   if (s != POP_OK) return s;
-  return down_tc(h, M, h->idx_all, h->N, Y, st);
+  return down_tc(h, M, h->idx_all, h->N, h->ch_s, 0, Y, st);
 }
 
 pop_status pop_get_partition(pop_ffn_t h, int* R, int* C, int* P) {

@@ -38,7 +38,9 @@ struct DecodeTcArgs {
   int K;                 // reduction extent: D (gate/up) or the kept items |R| + k (down)
   int N;                 // channel count, for the index guards
   const int* rc;         // gate/up: position -> channel ([C | R])
-  const int* ch_list;    // down: kept item -> channel (R, then S)
+  const int* ch_r;       // down: channels of the items j < nR_items (R)
+  const int* ch_s;       // down: channels of the items j >= nR_items (the selected candidates)
+  int nR_items;
   int nC;                // gate/up: positions below nC are candidates
   const float* n2;       // ||W2[:, c]||
   float* z;              // gate/up out: fp32 [B][ldz]
@@ -49,8 +51,7 @@ struct DecodeTcArgs {
   float* scores;         // gate/up out: [nC]
   void* y;               // down out: [B][D], fp32 or bf16
   int out_f32;
-  float* ws;             // stream-K partial accumulators, decode_tc_workspace_floats() floats
-  unsigned* tile_cnt;    // one counter per tile (0 between launches)
+  int split;             // CTAs per tile along K (a cluster); set by the launcher
   unsigned* err;
   uint64_t wait_ns;
 };
@@ -58,7 +59,6 @@ cudaError_t launch_gateup_tc(const CUtensorMap& x_map, const DecodeTcArgs& args,
 // zk_map / zk_lo_map: the hi and lo bf16 planes of z over the kept items
 cudaError_t launch_down_tc(const CUtensorMap& zk_map, const CUtensorMap& zk_lo_map, const DecodeTcArgs& args,
                            int num_sms, cudaStream_t st);
-size_t decode_tc_workspace_floats(int num_sms);
 
 // ---- decode step for B = 1 (pop_decode1.cu): gate/up with in-kernel top-k, tiled down
 struct DecodeB1Args {
@@ -101,12 +101,15 @@ cudaError_t launch_partition(const float* sumsq, const float* n2, float* I, int 
 // Candidate selection for one decode step (periodic memory, top-k, step counter).
 cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
                           unsigned* err, cudaStream_t st);
-// The same for B > 1, followed by the down projection's item lists: ch_list[j] = rc[nC + j] for
-// j < nR, ch_list[nR + j] = rc[S[j]], and the hi / lo bf16 parts of z[b][S[j]] at zk[b][nR + j] /
-// zk_lo[b][nR + j] for j < k, b < B. Launched with programmatic dependent launch.
-cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int nR, int k, int period, int* step,
-                             int* S, const int* rc, int* ch_list, const float* z, int ldz, int B, uint16_t* zk,
-                             uint16_t* zk_lo, int ldk, int N, unsigned* err, cudaStream_t st);
+// The same for B > 1 (the top-k only), launched with programmatic dependent launch.
+cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
+                             unsigned* err, cudaStream_t st);
+// The selected candidates' side of the B > 1 down projection: ch_s[j] = rc[S[j]] and the hi / lo
+// bf16 parts of z[b][S[j]] at zk[b][nR + j] / zk_lo[b][nR + j], for j < k, b < B. Many CTAs,
+// launched with programmatic dependent launch.
+cudaError_t launch_pack_selected(const int* S, int k, int nC, const int* rc, int N, int* ch_s, const float* z,
+                                 int ldz, int B, uint16_t* zk, uint16_t* zk_lo, int ldk, int nR, unsigned* err,
+                                 cudaStream_t st);
 // sumsq[i] (+)= sum over rows p < rows of part[p * ld + i], p ascending.
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
                               cudaStream_t st);
