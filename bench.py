@@ -410,14 +410,15 @@ def traffic_from_profiles(kernel: str, workload: str):
         text = open(path).read()
     except OSError:
         return None
-    src_name = "pop_decode1.cu" if workload.endswith("-b1") else "pop_decode.cu"
+    src_name = "pop_decode1.cu" if workload.endswith("-b1") else "pop_decode_tc.cu"
     src = open(os.path.join(ROOT, "online_structured_ffn_gb300", "csrc", src_name), "rb").read()
     sha = hashlib.sha256(src).hexdigest()[:16]
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256_16")):
+        line = line.strip().lstrip("-* ")
+        if ":" in line and line.startswith(("traffic_bytes_per_launch", "source_sha256_16")):
             k, v = line.split(":", 1)
-            vals[k.strip().lstrip("-* ").strip("`")] = v.strip().strip("`")
+            vals[k.strip().strip("`")] = v.strip().split()[0].strip("`")
     if vals.get("source_sha256_16") != sha:
         return None
     try:
