@@ -48,23 +48,27 @@ constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 constexpr uint64_t TC_DRAIN_NS = 1000000000ull;
 // shared memory for the stage ring (the down kernel also keeps its row-offset windows)
-constexpr uint32_t TC_RING_BUDGET[2] = {210 * 1024, 192 * 1024};
+constexpr uint32_t TC_RING_BUDGET[2] = {212 * 1024, 192 * 1024};
 // down: row offsets of the items of up to TC_WIN k-blocks, per producer warp (its 32 rows of each)
 constexpr int TC_WIN = 64;
 
-// Stage layout: A (weight rows) then B (token tile). Gate/up: A = 128 gate rows + 128 up rows of
-// 128 bytes, B = NP rows of x. Down: A = 64 items x 128 outputs (two 64-wide halves), B = the hi
-// and lo planes of z, NP rows each. As many stages as fit the budget (at most 8).
+// A stage holds KSUB consecutive 64-wide k-blocks ("sub-stages"), so that every gathered row is
+// read in KSUB x 128 contiguous bytes. Sub-stage layout: A (weight rows) then B (token tile).
+// Gate/up: A = 128 gate rows + 128 up rows of 128 bytes, B = NP rows of x. Down: A = 64 items x
+// 128 outputs (two 64-wide halves), B = the hi and lo planes of z, NP rows each. As many stages as
+// fit the budget (at most 8).
+constexpr int KSUB = 2;
 template <int MODE, int NP>
 struct TcCfg {
   static constexpr uint32_t A_BYTES = MODE == 0 ? 2 * TC_BM * TC_BK * 2 : TC_BM * TC_BK * 2;
   static constexpr uint32_t B_BYTES = (MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t SUB_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t STAGE_BYTES = KSUB * SUB_BYTES;
   static constexpr int STAGES = TC_RING_BUDGET[MODE] / STAGE_BYTES < 8 ? TC_RING_BUDGET[MODE] / STAGE_BYTES : 8;
   static constexpr uint32_t TMEM_COLS = 256;  // two accumulator buffers of 2 x NP <= 128 columns
   // partial accumulators exchanged in a cluster, fp32 per row: [g | u] (gate/up) or hi + lo (down)
   static constexpr int PCOLS = MODE == 0 ? 2 * NP : NP;
-  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  static_assert(SUB_BYTES % 1024 == 0, "sub-stages must keep the 1024-byte swizzle alignment");
   static_assert(static_cast<uint32_t>(TC_BM * PCOLS * 4) <= STAGES * STAGE_BYTES, "partials reuse the ring");
 };
 
@@ -153,14 +157,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (a.rows + TC_BM - 1) / TC_BM;
   const int KB = (a.K + TC_BK - 1) / TC_BK;
-  // this CTA's work: tiles unit, unit + nunits, ...; k-blocks [kb_lo, kb_hi) of each
+  const int KBS = (KB + KSUB - 1) / KSUB;  // stages per tile
+  // this CTA's work: tiles unit, unit + nunits, ...; stages [sb_lo, sb_hi) of each
   const int SK = a.split;
   const uint32_t rank = SK > 1 ? cluster_rank() : 0u;
   const int unit = static_cast<int>(blockIdx.x) / SK, nunits = static_cast<int>(gridDim.x) / SK;
-  const int kb_lo = static_cast<int>(rank) * KB / SK, kb_hi = (static_cast<int>(rank) + 1) * KB / SK;
+  const int sb_lo = static_cast<int>(rank) * KBS / SK, sb_hi = (static_cast<int>(rank) + 1) * KBS / SK;
+  const int kb_end = min(KB, sb_hi * KSUB);  // this CTA's k-blocks: [sb_lo * KSUB, kb_end)
   // bytes the TMA boxes bring per stage (the weight rows come by cp.async): NP token rows of x
   // (gate/up) or 2 x NP (the hi and lo planes of z, down)
-  const uint32_t tx_bytes = static_cast<uint32_t>(MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
+  const uint32_t tx_bytes = KSUB * static_cast<uint32_t>(MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int win_lo = -1, win_hi = -1;  // k-blocks [win_lo, win_hi) are in the window
     auto fill_window = [&](int kb0w) {
       win_lo = kb0w;
-      win_hi = min(kb_hi, kb0w + TC_WIN);
+      win_hi = min(kb_end, kb0w + TC_WIN);
       const int item_in_kb = 4 * warp + (lane & 3) + 8 * (lane >> 2);
       __syncwarp();
       for (int c0 = win_lo; c0 < win_hi; c0 += 16) {
@@ -256,12 +262,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         set_rows(ids);
       }
-      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+      for (int sbk = sb_lo; sbk < sb_hi; ++sbk) {
+        uint32_t rowsub[KSUB][MODE == 1 ? NROW : 1];  // down: row offsets of each sub-stage's items
         if (MODE == 1) {
-          if (kb < win_lo || kb >= win_hi) fill_window(kb);
-          const uint32_t* wrow = win + (kb - win_lo) * 32 + (rg - 4 * warp);
 #pragma unroll
-          for (int m = 0; m < NROW; ++m) rowoff[m] = wrow[4 * m];
+          for (int u = 0; u < KSUB; ++u) {
+            const int kb = sbk * KSUB + u;
+            if (kb < kb_end) {
+              if (kb < win_lo || kb >= win_hi) fill_window(kb);
+              const uint32_t* wrow = win + (kb - win_lo) * 32 + (rg - 4 * warp);
+#pragma unroll
+              for (int m = 0; m < NROW; ++m) rowsub[u][m % (MODE == 1 ? NROW : 1)] = wrow[4 * m];
+            } else {
+#pragma unroll
+              for (int m = 0; m < NROW; ++m) rowsub[u][m % (MODE == 1 ? NROW : 1)] = 0u;  // past K: zeros
+            }
+          }
         }
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1u;
@@ -277,28 +293,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           break;
         }
         const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        uint8_t* sb = smem + s * STAGE_BYTES + Cfg::A_BYTES;
         if (MODE == 0) {
-          const int d0 = kb * TC_BK + 8 * cq;
-          const uint32_t nbytes = d0 < a.D ? 16u : 0u;  // D is a multiple of 8: chunks are all in or all out
-          const uint16_t* base = Wbase + (nbytes ? d0 : 0);
+          // row by row, both k-blocks: KSUB x 128 contiguous bytes of each row back to back
 #pragma unroll
           for (int m = 0; m < NROW; ++m) {
             const int r = rg + 8 * m;
-            const uint32_t dst = sa + r * 128 + ((cq ^ (r & 7)) << 4);
-            cp_async16(dst, base + rowoff[m], nbytes);
-            cp_async16(dst + TC_BM * 128, base + rowoff[m] + a.D, nbytes);
+#pragma unroll
+            for (int u = 0; u < KSUB; ++u) {
+              const int d0 = (sbk * KSUB + u) * TC_BK + 8 * cq;
+              const uint32_t nbytes = d0 < a.D ? 16u : 0u;  // D is a multiple of 8: chunks all in or out
+              const uint16_t* src = Wbase + rowoff[m] + (nbytes ? d0 : 0);
+              const uint32_t dst = sa + u * Cfg::SUB_BYTES + r * 128 + ((cq ^ (r & 7)) << 4);
+              cp_async16(dst, src, nbytes);
+              cp_async16(dst + TC_BM * 128, src + a.D, nbytes);
+            }
           }
         } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int d0 = tile * TC_BM + 64 * h + 8 * cq;
-            const uint32_t nbytes = d0 < a.D ? 16u : 0u;
-            const uint16_t* base = Wbase + (nbytes ? d0 : 0);
+          for (int u = 0; u < KSUB; ++u) {
 #pragma unroll
-            for (int m = 0; m < NROW; ++m) {
-              const int r = rg + 8 * m;
-              cp_async16(sa + h * (TC_BK * 128) + r * 128 + ((cq ^ (r & 7)) << 4), base + rowoff[m], nbytes);
+            for (int h = 0; h < 2; ++h) {
+              const int d0 = tile * TC_BM + 64 * h + 8 * cq;
+              const uint32_t nbytes = d0 < a.D ? 16u : 0u;
+              const uint16_t* base = Wbase + (nbytes ? d0 : 0);
+#pragma unroll
+              for (int m = 0; m < NROW; ++m) {
+                const int r = rg + 8 * m;
+                cp_async16(sa + u * Cfg::SUB_BYTES + h * (TC_BK * 128) + r * 128 + ((cq ^ (r & 7)) << 4),
+                           base + rowsub[u][m % (MODE == 1 ? NROW : 1)], nbytes);
+              }
             }
           }
         }
@@ -309,8 +332,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           mbar_arrive(&ctl->full[(issued - LAG) % STAGES]);
         }
         if (warp == 0 && lane == 0) {
-          tma_load_2d(sb, &mapB, &ctl->full[s], kb * TC_BK, 0);
-          if (MODE == 1) tma_load_2d(sb + NP * 128, &mapB2, &ctl->full[s], kb * TC_BK, 0);  // z lo plane
+#pragma unroll
+          for (int u = 0; u < KSUB; ++u) {
+            uint8_t* sb = smem + s * STAGE_BYTES + u * Cfg::SUB_BYTES + Cfg::A_BYTES;
+            const int kx = (sbk * KSUB + u) * TC_BK;  // may lie past K: the box then reads zeros
+            tma_load_2d(sb, &mapB, &ctl->full[s], kx, 0);
+            if (MODE == 1) tma_load_2d(sb + NP * 128, &mapB2, &ctl->full[s], kx, 0);  // z lo plane
+          }
         }
         ++issued;
       }
@@ -344,7 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * HALF_COLS;
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        for (int sbk = sb_lo; sbk < sb_hi; ++sbk) {
           const int s = consumed % STAGES;
           const uint32_t ph = (consumed / STAGES) & 1u;
           if (!mbar_wait_bounded(&ctl->full[s], ph, a.wait_ns, abort_flag)) {
@@ -353,18 +381,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < TC_BK / 16; ++k) {
-            const uint32_t acc = (kb > kb_lo || k > 0) ? 1u : 0u;
-            const uint64_t bdesc = smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-            if (MODE == 0) {
-              umma_f16(d_tmem, smem_desc_sw128(sa + 32u * k, 16u, 1024u), bdesc, idesc, acc);
-              umma_f16(d_tmem + static_cast<uint32_t>(NP), smem_desc_sw128(sa + TC_BM * 128 + 32u * k, 16u, 1024u),
-                       bdesc, idesc, acc);
-            } else {
-              umma_f16(d_tmem, smem_desc_sw128(sa + 2048u * k, TC_BK * 128, 1024u), bdesc, idesc, acc);
+          for (int u = 0; u < KSUB; ++u) {
+            const uint32_t sa = smem_u32(smem + s * STAGE_BYTES) + u * Cfg::SUB_BYTES;
+            const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k) {
+              const uint32_t acc = (sbk > sb_lo || u > 0 || k > 0) ? 1u : 0u;
+              const uint64_t bdesc = smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+              if (MODE == 0) {
+                umma_f16(d_tmem, smem_desc_sw128(sa + 32u * k, 16u, 1024u), bdesc, idesc, acc);
+                umma_f16(d_tmem + static_cast<uint32_t>(NP),
+                         smem_desc_sw128(sa + TC_BM * 128 + 32u * k, 16u, 1024u), bdesc, idesc, acc);
+              } else {
+                umma_f16(d_tmem, smem_desc_sw128(sa + 2048u * k, TC_BK * 128, 1024u), bdesc, idesc, acc);
+              }
             }
           }
           umma_commit(&ctl->empty[s]);
@@ -582,6 +613,7 @@ static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, Dec
   }
   const int tiles = (args.rows + TC_BM - 1) / TC_BM;
   const int KB = (args.K + TC_BK - 1) / TC_BK;
+  const int KBS = (KB + KSUB - 1) / KSUB;
   if (tiles <= 0 || KB <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg{};
   cfg.blockDim = dim3(TC_THREADS);
@@ -595,7 +627,7 @@ static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, Dec
   // split: the largest power of two <= 8 such that tiles x split CTAs fit the SMs at once (one CTA
   // per SM) with at least one k-block per CTA, confirmed by the cluster occupancy query
   int split = 1;
-  while (split < 8 && tiles * split * 2 <= num_sms && split * 2 <= KB) split *= 2;
+  while (split < 8 && tiles * split * 2 <= num_sms && split * 2 <= KBS) split *= 2;
   for (; split > 1; split /= 2) {
     attr[1].val.clusterDim.x = split;
     attr[1].val.clusterDim.y = 1;
