@@ -202,9 +202,9 @@ class Stack:
     def launches_per_session(self):
         # prefill: per chunk gate/up GEMM + sum fold + down GEMM, then the partition kernel;
         # decode at B = 1: gate/up with the top-k inside (+ a separate top-k when |C| > 8192) and the
-        # tiled down projection; at B > 1: gate/up, selection, down, reduction
+        # tiled down projection; at B > 1: gate/up with the selection inside, and the down GEMM
         c = self.counts
-        per_step = (2 + (1 if c.n_C > 8192 else 0)) if self.wl["B"] == 1 else 4
+        per_step = (2 + (1 if c.n_C > 8192 else 0)) if self.wl["B"] == 1 else 2
         per_layer = 3 * self.chunks + 1 + per_step * self.wl["T"]
         return per_layer * self.wl["layers"]
 
@@ -501,7 +501,7 @@ def main():
         "config": config,
         "roofline": {"bound": "hbm",
                      "kernel": ("k_gateup_sel_b1 (decode gate/up over R u C, top-k inside)" if wl["B"] == 1
-                                else "k_gateup_mma (decode gate/up over R u C, B > 1)"),
+                                else "k_gateup_tc (decode gate/up over R u C on tcgen05, top-k inside, B > 1)"),
                      "achieved": res["gateup_gbs"], "peak": res["peak"], "unit": "GB/s",
                      "frac": res["gateup_gbs"] / res["peak"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": res["roof_bytes"], "peak_source": res["peak_kind"]},

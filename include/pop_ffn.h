@@ -127,10 +127,10 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
  * x: device bf16 [B, D], 1 <= B <= max_batch; y: device [B, D] (float32 if out_f32 else bf16).
  * Computes z over R u C, candidate scores a_i = max_b |z_{b,i}| * ||W2[:,i]||, updates the memory,
  * selects the k best candidates when step % period == 0 (ties to the lower index), and writes
- * y = sum over R u S of z_i * W2[:,i]. No allocation and no host synchronization. At B = 1 the
- * step is two kernels launched with programmatic dependent launch (the next kernel's weight
- * prefetch overlaps the previous kernel's tail); each waits for its predecessor before it touches
- * data a previous call may still use.
+ * y = sum over R u S of z_i * W2[:,i]. No allocation and no host synchronization. The step is two
+ * kernels launched with programmatic dependent launch (gate/up with the selection inside, then the
+ * down projection; the next kernel's weight loads overlap the previous kernel's tail); each waits
+ * for its predecessor before it touches data a previous call may still use.
  * STATE if no partition has been set. */
 pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* stream);
 

@@ -1,10 +1,11 @@
-// Decode step of the POP FFN for B > 1 sequences on the 5th-generation tensor cores.
+// Decode step of the POP FFN for B > 1 sequences on the 5th-generation tensor cores: two launches.
 //
 // What it computes ("POP: Online Structural Pruning..." notes, Key design 2; "Batch-wise adaptive
-// pruning", Fig. 2(a) for the batch max):
+// pruning", Fig. 2(a) for the batch max and the abstract for the periodic memory):
 //   gate/up: for every position p of rc = [C | R] and token b, z[b][p] = SiLU(Wg[c] x_b) * (W1[c] x_b)
 //            with c = rc[p]; score[p] = max_b |z[b][p]| * ||W2[:, c]|| for the candidates p < |C|;
-//   down:    y[b][d] = sum over the kept items j (R, then S) of z[b][j] * W2[d, channel of j].
+//   down:    the memory update and the top-k over C (every `period` steps), then
+//            y[b][d] = sum over the kept items j (R, then the selected S) of z[b][j] * W2[d, channel of j].
 //
 // The MMA inputs are bf16. x and the weights are bf16 already; z is not, and rounding it to bf16
 // would cost about 3 significant digits of y. So the down GEMM takes z as two bf16 planes, hi =
@@ -12,83 +13,93 @@
 // the two halves, which leaves z's own fp32 rounding well below the output tolerance.
 //
 // Both are skinny GEMMs with the tokens as the MMA's N (16..64, zero-padded to a multiple of 16)
-// and 128 rows as M: 128 positions (gate/up; the A tiles are gathered rows of the packed weights,
-// K-major) or 128 outputs d (down; A is gathered down columns, MN-major since d is contiguous in a
-// packed row). The producer warps gather the rows straight from the packed weights with 16-byte
-// cp.async copies into the 128-byte swizzle layout (no copy of the pruned weights is ever made;
-// TMA's four-row gather moved too few bytes per operation to keep up with HBM here). The x (or z)
-// tile is an ordinary TMA box.
+// and 128 rows as M. Eight producer warps gather the pruned weight rows straight from the packed
+// weights with 16-byte cp.async copies into the 128-byte swizzle layout (no copy of the pruned
+// weights is ever made). Measured on this part: the gather reaches ~6.2 TB/s with eight producer
+// warps against ~2-4 TB/s with two, and an MMA of M = 128, K = 16 costs ~44 cycles for N <= 32
+// whatever its rows hold, so each MMA should carry as many real rows as it can. A copy's landing
+// arrives on its stage's barrier by itself (cp.async.mbarrier.arrive), so a producer only ever
+// waits for a free slot; the MMA thread fences the landed copies for the tensor cores after its
+// barrier wait.
 //
-// Work split. With few tiles (the usual decode shapes: |R u C| / 128 or D / 128 is well below the
-// SM count) every tile is split along K over a cluster of `split` CTAs (1 CTA per SM, 2 / 4 / 8 per
-// cluster); each CTA streams 1/split of the tile's k-blocks, then the partial accumulators are
-// added through distributed shared memory in rank order (a fixed order: results do not depend on
-// timing), each CTA finishing 128 / split of the rows. No workspace, no atomics. With many tiles
-// (split = 1), CTAs take whole tiles round-robin and finish them straight from TMEM.
+// Gate/up (k_gateup_tc): one CTA per SM; each CTA streams "units" of at most 64 positions over all
+// of K. The unit ranges are ragged (P / units each) so that the number of units matches the number
+// of CTAs. One MMA covers gate and up of a unit together: TMEM lane quarter q holds gate rows
+// 16q..16q+15 in lanes 0-15 and the up rows of the same positions in lanes 16-31, so an epilogue
+// warp pairs them with one shuffle. Rows past a unit's end are never written and the accumulator
+// rows they produce are never read: row m of an MMA result depends on row m of A only. A stage
+// holds 4 (or 2) consecutive k-blocks, so each gathered row is read in 512 (256) contiguous bytes.
+// Weight rows and the partition are constant between partitions, so a CTA starts filling its ring
+// before griddepcontrol.wait; only the x boxes and the stores of this step's data wait for the
+// previous kernel.
 //
-// Roles (224 threads): warps 0-1 issue the copies, warp 2 lane 0 issues the MMAs and owns TMEM
-// (two accumulator buffers, so the epilogue of one tile overlaps the MMAs of the next), warps 3-6
-// are the epilogue (one TMEM lane quarter each). Every wait is bounded; on a time-out the CTA
-// records DEVERR_TIMEOUT_DECODE_TC, stops issuing, drains its own copies and MMAs (bounded), frees
-// TMEM and returns. The epilogue warps take every decision that guards a named barrier together,
-// and every thread reaches the cluster barriers, so a time-out cannot leave a barrier waiting.
+// Down (k_down_tc): each unit (at most 128 outputs) is split along K over a cluster of `split`
+// CTAs; every CTA streams its share of the R items first, then its share of the selected items.
+// The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
+// writes the selected channels and their z planes, and releases a flag; the other CTAs wait
+// (bounded) for the flag only when they reach their first selected item. The partial accumulators
+// of a split unit are added through distributed shared memory in rank order (a fixed order:
+// results do not depend on timing). No workspace, no atomics on data.
 //
-// Programmatic dependent launch: the set-up (barriers, TMEM, tensor-map prefetch) runs before
-// griddepcontrol.wait; every global read or write of this step's data comes after it.
+// Roles (416 threads): warps 0-7 gather, warp 8 lane 0 issues the MMAs and owns TMEM (two
+// accumulator buffers, so the epilogue of one unit overlaps the MMAs of the next), warps 9-12 are
+// the epilogue (TMEM lane quarter = warp % 4). Every wait is bounded; on a time-out the CTA records
+// DEVERR_TIMEOUT_DECODE_TC, stops issuing, drains its own copies and MMAs (bounded), frees TMEM and
+// returns. The warps of a role take every decision that guards a named barrier together, and every
+// thread reaches the cluster barriers, so a time-out cannot leave a barrier waiting.
 #include "pop_device.cuh"
 #include "pop_internal.h"
+#include "pop_radix.cuh"
 
 namespace pop {
 
 namespace {
-constexpr int TC_THREADS = 224;
-constexpr int TC_PRODUCERS = 2;  // warps 0-1 gather rows, warp 2 issues MMAs, warps 3-6 are the epilogue
-constexpr int TC_MMA_WARP = TC_PRODUCERS;
+constexpr int TC_PW = 8;             // producer warps 0..7
+constexpr int TC_MMA_WARP = TC_PW;   // warp 8
+constexpr int TC_EPI0 = TC_PW + 1;   // warps 9..12
+constexpr int TC_THREADS = 32 * (TC_PW + 5);
+constexpr int TC_PROD_THREADS = 32 * TC_PW;
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
+constexpr int TC_MAX_STAGES = 16;
 constexpr uint64_t TC_DRAIN_NS = 1000000000ull;
-// shared memory for the stage ring (the down kernel also keeps its row-offset windows)
-constexpr uint32_t TC_RING_BUDGET[2] = {212 * 1024, 192 * 1024};
-// down: row offsets of the items of up to TC_WIN k-blocks, per producer warp (its 32 rows of each)
-constexpr int TC_WIN = 64;
+constexpr uint32_t TC_TMEM_COLS = 256;  // two accumulator buffers of <= 128 fp32 columns
+constexpr uint32_t TC_HALF = TC_TMEM_COLS / 2;
+constexpr uint32_t TC_RING = 192 * 1024;
+constexpr int GU_MAX_ROWS = 64;  // positions per unit (gate + up = 128 MMA rows)
+// down: per producer warp, the channels of its 8 items of each of DN_WIN k-blocks
+constexpr int DN_WIN = 32;
+constexpr int DN_WIN_WORDS = 8 * DN_WIN * 8;
+constexpr int DN_PRE = 2;  // stages of down columns issued before waiting for the previous kernel
+constexpr int GU_PRE = 2;         // stages of weights issued before waiting for the previous kernel
 
-// A stage holds KS = 2 consecutive 64-wide k-blocks ("sub-stages"): gate/up rows are then read in
-// 256 contiguous bytes (measured faster than 128), and the down GEMM's per-stage overhead is halved
-// (4 k-blocks per stage measured slower: fewer, larger stages). Sub-stage layout: A (weight rows) then B (token tile).
-// Gate/up: A = 128 gate rows + 128 up rows of 128 bytes, B = NP rows of x. Down: A = 64 items x
-// 128 outputs (two 64-wide halves), B = the hi and lo planes of z, NP rows each. As many stages as
-// fit the budget (at most 8).
-template <int MODE, int NP>
-struct TcCfg {
-  static constexpr int KS = 2;
-  static constexpr uint32_t A_BYTES = MODE == 0 ? 2 * TC_BM * TC_BK * 2 : TC_BM * TC_BK * 2;
-  static constexpr uint32_t B_BYTES = (MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
-  static constexpr uint32_t SUB_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t STAGE_BYTES = KS * SUB_BYTES;
-  static constexpr int STAGES = TC_RING_BUDGET[MODE] / STAGE_BYTES < 8 ? TC_RING_BUDGET[MODE] / STAGE_BYTES : 8;
-  static constexpr uint32_t TMEM_COLS = 256;  // two accumulator buffers of 2 x NP <= 128 columns
-  // partial accumulators exchanged in a cluster, fp32 per row: [g | u] (gate/up) or hi + lo (down)
-  static constexpr int PCOLS = MODE == 0 ? 2 * NP : NP;
-  static_assert(SUB_BYTES % 1024 == 0, "sub-stages must keep the 1024-byte swizzle alignment");
-  static_assert(static_cast<uint32_t>(TC_BM * PCOLS * 4) <= STAGES * STAGE_BYTES, "partials reuse the ring");
+// Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major), B = the hi
+// and lo planes of z, NP rows each.
+template <int NP>
+struct DnCfg {
+  static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+  static constexpr uint32_t B_BYTES = 2 * NP * TC_BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = TC_RING / STAGE_BYTES < 12 ? TC_RING / STAGE_BYTES : 12;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  static_assert(static_cast<uint32_t>(TC_BM * NP * 4) <= STAGES * STAGE_BYTES, "partials reuse the ring");
 };
 
 struct TcCtl {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[TC_MAX_STAGES];
+  uint64_t empty[TC_MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int seg_ok[2];  // by tile parity: a warp may still read one while the next is written
-  float n2s[TC_BM];                 // gate/up, split tiles: norms of the rows each epilogue thread finishes
+  int seg_ok[2];  // by unit parity: a warp may still read one while the next is written
+  unsigned sel_seen;  // down: the selection epoch warp 0 has seen complete
 };
 
-template <int MODE, int NP>
-constexpr size_t tc_smem_bytes() {
-  return 1024 + TcCfg<MODE, NP>::STAGES * TcCfg<MODE, NP>::STAGE_BYTES + sizeof(TcCtl) +
-         (MODE == 1 ? TC_PRODUCERS * TC_WIN * 32 * sizeof(uint32_t) : 0);
+template <int NP>
+constexpr size_t dn_smem_bytes() {
+  return 1024 + DnCfg<NP>::STAGES * DnCfg<NP>::STAGE_BYTES;
 }
 
 __device__ __forceinline__ float silu_t(float g) { return g / (1.0f + expf(-g)); }
@@ -101,22 +112,43 @@ __device__ __forceinline__ int guard_ch(int v, int n, unsigned* err) {
   return v;
 }
 
+__device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+  hi = *reinterpret_cast<const uint16_t*>(&h);
+  lo = *reinterpret_cast<const uint16_t*>(&l);
+}
+
 // 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros (nothing is read). No
-// compiler memory barrier: the source is read-only and the destination is touched by nothing else
-// of this thread before the commit / wait below, which do carry one; so the address arithmetic
-// of consecutive copies can overlap.
+// compiler memory barrier: the source is read-only for this kernel and the destination is touched
+// by nothing else of this thread.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Waits until every cp.async this thread has issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Arrives on `bar` once every cp.async this thread has issued so far has landed (the arrival
+// counts toward the barrier's initial count). The thread itself does not wait.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Makes this thread's shared-memory writes (its landed cp.async copies) visible to the tensor cores.
+// Orders shared-memory writes of the generic proxy (landed cp.async copies, made visible to this
+// thread by a barrier wait) before this thread's later tensor-core reads of them (async proxy).
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void prod_bar() { asm volatile("bar.sync 2, %0;" ::"n"(TC_PROD_THREADS) : "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // All threads of all CTAs of the cluster; orders shared-memory writes before the barrier with
 // (distributed) shared-memory reads after it.
@@ -139,62 +171,173 @@ __device__ __forceinline__ float2 ld_peer2(uint32_t addr) {
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
   return v;
 }
+
+// barrier over the eight producer warps (the selecting CTA uses the same warps)
+struct ProdSync {
+  __device__ void operator()() const { prod_bar(); }
+};
+
+// ------------------------------------------------------------------ selection (down, first cluster)
+// Updates the periodic memory and selects the k best candidates when the step is an update step
+// (select_step, warps 0-7), then, with all 416 threads, writes the selected candidates' channels and
+// the hi / lo bf16 parts of their z at columns 64 * kbr + j of the z planes, advances the step
+// counter and releases the flag. S is kept in shared memory next to the keys when both fit.
+__device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_PROD_THREADS>& rsc) {
+  // While the GEMM CTAs stream, every global access of this CTA waits behind their requests
+  // (microseconds), so all inputs are fetched in one round at the start, into shared memory:
+  //   [keys: nC u32 | scores: nC f32 | channels of C: nC i32 | S: k i32 | z of C: nC x ldzc f32]
+  // (z only when it fits; otherwise the pack reads it from global memory).
+  const int tid = threadIdx.x;
+  const int nC = a.nC, k = a.k;
+  uint32_t dyn = 0;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+  const size_t avail = dyn > 1024 ? dyn - 1024 : 0;
+  auto al16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+  const size_t o_keys = 0, o_sc = al16(static_cast<size_t>(nC) * 4), o_rc = o_sc + al16(static_cast<size_t>(nC) * 4);
+  const size_t o_S = o_rc + al16(static_cast<size_t>(nC) * 4), o_z = o_S + al16(static_cast<size_t>(k) * 4);
+  const bool small = o_z <= avail;  // scores, channels and S in shared memory
+  const bool zin = small && o_z + static_cast<size_t>(nC) * a.ldzc * 4 <= avail;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + o_keys);
+  float* s_sc = reinterpret_cast<float*>(smem + o_sc);
+  int* s_rc = reinterpret_cast<int*>(smem + o_rc);
+  int* sS = small ? reinterpret_cast<int*>(smem + o_S) : a.S;
+  float* s_z = reinterpret_cast<float*>(smem + o_z);
+  const int t = *a.step;
+  const bool update = (t % a.period) == 0;
+  if (small) {
+    const uint32_t sb = smem_u32(smem);
+    for (int i = tid; i < (nC + 3) / 4; i += TC_THREADS) {
+      const int n = min(4, nC - 4 * i);
+      cp_async16(sb + static_cast<uint32_t>(o_sc) + 16u * i, a.scores + 4 * i, 4u * n);
+      cp_async16(sb + static_cast<uint32_t>(o_rc) + 16u * i, a.rc + 4 * i, 4u * n);
+    }
+    if (!update)  // the held selection of the last update step
+      for (int i = tid; i < (k + 3) / 4; i += TC_THREADS)
+        cp_async16(sb + static_cast<uint32_t>(o_S) + 16u * i, a.S + 4 * i, 4u * min(4, k - 4 * i));
+    if (zin) {
+      const int nz = nC * (a.ldzc / 4);  // ldzc is a multiple of 4: whole 16-byte chunks
+      for (int i = tid; i < nz; i += TC_THREADS) cp_async16(sb + static_cast<uint32_t>(o_z) + 16u * i, a.zc + 4 * i, 16u);
+    }
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  __shared__ int s_sel;
+  if (tid < TC_PROD_THREADS) {
+    bool sel = true;
+    if (nC > 0)
+      sel = select_step<TC_PROD_THREADS>(
+          tid, [&](int i) { return small ? s_sc[i] : __ldcg(a.scores + i); }, a.memory, nC, k, a.period, update, keys,
+          sS, rsc, ProdSync());
+    if (tid == 0) s_sel = sel ? 1 : 0;
+  }
+  __syncthreads();
+  if (update && small)
+    for (int j = tid; j < k; j += TC_THREADS) a.S[j] = sS[j];
+  // channels of the selected candidates
+  for (int j = tid; j < k; j += TC_THREADS) {
+    int ps = sS[j];
+    if (static_cast<unsigned>(ps) >= static_cast<unsigned>(nC)) {
+      atomicOr(a.err, DEVERR_INDEX);
+      ps = 0;
+      sS[j] = 0;
+    }
+    a.ch_s[j] = guard_ch(small ? s_rc[ps] : __ldg(a.rc + ps), a.N, a.err);
+  }
+  __syncthreads();
+  // z planes of the selected items: task (8 items from j0 = 8 o, 4 tokens from 4 q): eight float4
+  // reads of z, then per token one 16-byte store of eight hi parts and one of eight lo parts
+  uint16_t* zk = const_cast<uint16_t*>(a.zk);
+  uint16_t* zk_lo = zk + a.zk_lo_off;
+  const int col0 = 64 * a.kbr;
+  const int nq = a.ldzc >> 2, no = (k + 7) >> 3;
+  const int tasks = no * nq;
+  for (int e = tid; e < tasks; e += TC_THREADS) {
+    const int o = e % no, q = e / no;
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = 8 * o + i;
+      const size_t zo = j < k ? static_cast<size_t>(sS[j]) * a.ldzc + 4 * q : 0;
+      v[i] = j >= k ? make_float4(0.f, 0.f, 0.f, 0.f)
+                    : (zin ? *reinterpret_cast<const float4*>(s_z + zo) : __ldcg(reinterpret_cast<const float4*>(a.zc + zo)));
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int b = 4 * q + c;
+      if (b >= a.B) break;
+      uint16_t hi[8], lo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float f = c == 0 ? v[i].x : (c == 1 ? v[i].y : (c == 2 ? v[i].z : v[i].w));
+        split_bf16(f, hi[i], lo[i]);
+      }
+      const size_t off = static_cast<size_t>(b) * a.ldk + col0 + 8 * o;
+      *reinterpret_cast<uint4*>(zk + off) =
+          make_uint4(hi[0] | (uint32_t(hi[1]) << 16), hi[2] | (uint32_t(hi[3]) << 16), hi[4] | (uint32_t(hi[5]) << 16),
+                     hi[6] | (uint32_t(hi[7]) << 16));
+      *reinterpret_cast<uint4*>(zk_lo + off) =
+          make_uint4(lo[0] | (uint32_t(lo[1]) << 16), lo[2] | (uint32_t(lo[3]) << 16), lo[4] | (uint32_t(lo[5]) << 16),
+                     lo[6] | (uint32_t(lo[7]) << 16));
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (!s_sel) atomicOr(a.err, DEVERR_TOPK);
+    if (a.count_step) *a.step = t + 1;
+    __threadfence();
+    st_release_u32(a.flag, a.epoch);
+  }
+}
 }  // namespace
 
+// ------------------------------------------------------------------ gate/up over R u C
 // NP: tokens padded to a multiple of 16 (16..64), a template parameter so that every per-token
-// loop of the epilogue has a fixed trip count (no per-column branches between its loads).
-template <int MODE, int NP>
+// loop of the epilogue has a fixed trip count.
+template <int NP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    k_decode_tc(const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapB2,
-                const __grid_constant__ DecodeTcArgs a) {
-  using Cfg = TcCfg<MODE, NP>;
-  constexpr int STAGES = Cfg::STAGES;
-  constexpr uint32_t STAGE_BYTES = Cfg::STAGE_BYTES;
-  constexpr uint32_t HALF_COLS = Cfg::TMEM_COLS / 2;
+    k_gateup_tc(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ GateUpTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ TcCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  TcCtl* ctl = reinterpret_cast<TcCtl*>(smem + STAGES * STAGE_BYTES);
-  volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = (a.rows + TC_BM - 1) / TC_BM;
-  const int KB = (a.K + TC_BK - 1) / TC_BK;
-  constexpr int KSUB = Cfg::KS;
-  const int KBS = (KB + KSUB - 1) / KSUB;  // stages per tile
-  // this CTA's work: tiles unit, unit + nunits, ...; stages [sb_lo, sb_hi) of each
-  const int SK = a.split;
-  const uint32_t rank = SK > 1 ? cluster_rank() : 0u;
-  const int unit = static_cast<int>(blockIdx.x) / SK, nunits = static_cast<int>(gridDim.x) / SK;
-  const int sb_lo = static_cast<int>(rank) * KBS / SK, sb_hi = (static_cast<int>(rank) + 1) * KBS / SK;
-  const int kb_end = min(KB, sb_hi * KSUB);  // this CTA's k-blocks: [sb_lo * KSUB, kb_end)
-  // bytes the TMA boxes bring per stage (the weight rows come by cp.async): NP token rows of x
-  // (gate/up) or 2 x NP (the hi and lo planes of z, down)
-  const uint32_t tx_bytes = KSUB * static_cast<uint32_t>(MODE == 0 ? NP : 2 * NP) * TC_BK * 2;
+  const int W = static_cast<int>(gridDim.x), w = static_cast<int>(blockIdx.x);
+  const int U = a.units;
+  const int P = a.nC + a.nR;
+  const int RC = a.rows_cap;  // multiple of 16, <= 64
+  const int KS = a.ks;        // k-blocks per stage
+  const uint32_t AROWS = 2 * RC;
+  const uint32_t SUB = (AROWS + NP) * 128u;  // one k-block: A rows (gate and up interleaved) | x rows
+  const uint32_t STAGE = KS * SUB;
+  const int STAGES = a.stages;
+  const int KB = (a.D + TC_BK - 1) / TC_BK;
+  const int KBS = (KB + KS - 1) / KS;  // stages per unit
+  const uint32_t tx_bytes = KS * NP * TC_BK * 2;
+  auto unit_lo = [&](int u) { return static_cast<int>(static_cast<long long>(u) * P / U); };
+  volatile int* abort_flag = &ctl.abort_flag;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctl->full[s], 32 * TC_PRODUCERS + 1);  // producer lanes + the TMA transaction count
-      mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl.full[s], TC_PROD_THREADS + 1);  // producer lanes + the x box's arrival with its bytes
+      mbar_init(&ctl.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&ctl->tfull[b], 1);
-      mbar_init(&ctl->tempty[b], 4);
+      mbar_init(&ctl.tfull[b], 1);
+      mbar_init(&ctl.tempty[b], 4);
     }
-    mbar_init(&ctl->drain, 1);
-    ctl->abort_flag = 0;
+    mbar_init(&ctl.drain, 1);
+    ctl.abort_flag = 0;
     fence_mbar_init();
-    if (MODE == 1) prefetch_tmap(&mapB2);
-    prefetch_tmap(&mapB);
+    prefetch_tmap(&mapX);
   }
   if (warp == TC_MMA_WARP) {
-    tmem_alloc(&ctl->tmem_base, Cfg::TMEM_COLS);
+    tmem_alloc(&ctl.tmem_base, TC_TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = ctl->tmem_base;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t tmem_base = ctl.tmem_base;
+  pdl_trigger();  // the down kernel only starts where this grid's CTAs have left an SM
 
   auto fail = [&]() {
     if (!*abort_flag) {
@@ -203,91 +346,435 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   };
 
-  if (warp < TC_PRODUCERS) {
-    // ------------------------------------------------------------ producers (two whole warps)
-    // The weight rows of a stage are gathered with 16-byte cp.async copies (lane l of producer warp
-    // w copies chunk l % 8 of rows rg, rg + 8, ... with rg = l / 8 + 4 w), each written to its place
-    // in the 128-byte swizzle pattern; the token tile (x, or the two z planes) is a TMA box issued
-    // by warp 0. One commit group per stage: once a lane's group for stage i has landed (checked LAG
-    // stages later, so LAG + 1 stages of copies stay in flight) the lane fences its writes for the
-    // async proxy and arrives on the stage's barrier; warp 0 lane 0 also arrives with the TMA byte
-    // count when it issues the box.
-    const int cq = lane & 7, rg = (lane >> 3) + 4 * warp;
-    constexpr int LAG = STAGES - 1;
-    const uint16_t* Wbase = a.Wp + (MODE == 0 ? 0 : 2 * static_cast<size_t>(a.D));
-    const size_t row3 = 3 * static_cast<size_t>(a.D);
-    uint32_t issued = 0;
-    bool ok = true;
-    // Down: the row offsets of the items this warp copies (rows rg + 8m of each k-block), for a
-    // window of up to TC_WIN k-blocks at a time, in shared memory. Lane l of warp w fetches item
-    // (4w + l % 4) + 8 (l / 4) of each k-block of the window (one load per k-block, all in flight at
-    // once); the lane that copies rows rg + 8m reads entry (rg - 4w) + 4m. Each warp fills and reads
-    // only its own table, so the warps never wait on each other.
-    uint32_t* win = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(TcCtl)) +
-                    warp * TC_WIN * 32;
-    int win_lo = -1, win_hi = -1;  // k-blocks [win_lo, win_hi) are in the window
-    auto fill_window = [&](int kb0w) {
-      win_lo = kb0w;
-      win_hi = min(kb_end, kb0w + TC_WIN);
-      const int item_in_kb = 4 * warp + (lane & 3) + 8 * (lane >> 2);
-      __syncwarp();
-      for (int c0 = win_lo; c0 < win_hi; c0 += 16) {
-        int v[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int item = (c0 + u) * TC_BK + item_in_kb;
-          v[u] = 0;
-          if (c0 + u < win_hi && item < a.K) v[u] = item < a.nR_items ? a.ch_r[item] : a.ch_s[item - a.nR_items];
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (c0 + u < win_hi) win[(c0 + u - win_lo) * 32 + lane] = static_cast<uint32_t>(guard_ch(v[u], a.N, a.err)) * row3;
-      }
-      __syncwarp();
+  if (warp < TC_PW) {
+    // ------------------------------------------------------------ producers (eight warps)
+    // A stage is KS consecutive k-blocks of the unit's rows. Lane group `grp` (8 lanes) copies the
+    // rows (position j, gate/up g) numbered r = 2 j + g = grp, grp + 32, ... (at most 4 of them), each
+    // lane 16-byte chunk cq of every k-block of the stage, so one warp instruction reads 128-byte
+    // runs of four different rows (measured ~45% faster than one 512-byte run of one row per
+    // instruction) and a lane walks KS x 128 contiguous bytes of its row. The rows a lane copies are
+    // the same in every stage of a unit: their offsets and shared-memory places are computed once.
+    // Warp 0 lane 0 adds the x boxes: for the first GU_PRE stages after griddepcontrol.wait (the
+    // weights of those stages are already streaming by then), afterwards with each stage.
+    const int cq = lane & 7, grp = (warp * 32 + lane) >> 3;
+    const uint32_t row3 = 3u * static_cast<uint32_t>(a.D);  // 3 * D * D_FF < 2^32 under the size limits
+    const bool tma_lane = warp == 0 && lane == 0;
+    uint32_t issued = 0, x_done = 0;  // x boxes issued for stages [0, x_done)
+    bool ok = true, waited = false;
+    auto issue_x = [&](uint32_t i) {
+      const int s = static_cast<int>(i % static_cast<uint32_t>(STAGES));
+      const int sbk = static_cast<int>(i % static_cast<uint32_t>(KBS));
+      mbar_arrive_expect_tx(&ctl.full[s], tx_bytes);
+      for (int u = 0; u < KS; ++u)
+        tma_load_2d(smem + s * STAGE + u * SUB + AROWS * 128, &mapX, &ctl.full[s], (sbk * KS + u) * TC_BK, 0);
     };
-    for (int tile = unit; tile < tiles && ok; tile += nunits) {
-      // MODE 0: the tile's 128 rows are positions 128 * tile + r; this lane copies rows rg + 8m.
-      // MODE 1: the k-block's 64 rows are items 64 * kb + r; this lane copies items rg + 8m.
-      // Row offsets (elements) stay in registers.
-      constexpr int NROW = MODE == 0 ? TC_BM / 8 : TC_BK / 8;
-      uint32_t rowoff[NROW];
-      auto set_rows = [&](const int (&ids)[NROW]) {
+    for (int u = w; u < U && ok; u += W) {
+      const int lo = unit_lo(u), nrows = unit_lo(u + 1) - lo;
+      uint32_t rowbase[4], dst[4];
 #pragma unroll
-        for (int m = 0; m < NROW; ++m) rowoff[m] = static_cast<uint32_t>(guard_ch(ids[m], a.N, a.err)) * row3;
-      };
-      if (MODE == 0) {
-        int ids[NROW];
-#pragma unroll
-        for (int m = 0; m < NROW; ++m) {
-          const int p = tile * TC_BM + rg + 8 * m;
-          ids[m] = p < a.rows ? a.rc[p] : 0;
+      for (int t = 0; t < 4; ++t) {
+        const int rr = grp + 32 * t;  // row 2 j + g of the unit
+        rowbase[t] = 0xffffffffu;
+        dst[t] = 0u;
+        if (rr < 2 * nrows) {
+          const int g = rr & 1, j = rr >> 1;
+          const int ch = guard_ch(__ldg(a.rc + lo + j), a.N, a.err);
+          const int arow = 32 * (j >> 4) + 16 * g + (j & 15);
+          rowbase[t] = static_cast<uint32_t>(ch) * row3 + static_cast<uint32_t>(g) * a.D + 8 * cq;
+          dst[t] = arow * 128 + ((cq ^ (arow & 7)) << 4);
         }
-        set_rows(ids);
       }
-      for (int sbk = sb_lo; sbk < sb_hi; ++sbk) {
-        uint32_t rowsub[KSUB][MODE == 1 ? NROW : 1];  // down: row offsets of each sub-stage's items
-        if (MODE == 1) {
+      for (int sbk = 0; sbk < KBS; ++sbk) {
+        const int s = static_cast<int>(issued % static_cast<uint32_t>(STAGES));
+        const uint32_t ph = (issued / static_cast<uint32_t>(STAGES)) & 1u;
+        bool got = true;
+        if (lane == 0) {
+          got = mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, a.wait_ns, abort_flag);
+          if (!got) fail();
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(smem + s * STAGE);
+        const uint32_t kbase = static_cast<uint32_t>(sbk * KS * TC_BK);
 #pragma unroll
-          for (int u = 0; u < KSUB; ++u) {
-            const int kb = sbk * KSUB + u;
-            if (kb < kb_end) {
-              if (kb < win_lo || kb >= win_hi) fill_window(kb);
-              const uint32_t* wrow = win + (kb - win_lo) * 32 + (rg - 4 * warp);
+        for (int t = 0; t < 4; ++t) {
+          if (rowbase[t] != 0xffffffffu) {
 #pragma unroll
-              for (int m = 0; m < NROW; ++m) rowsub[u][m % (MODE == 1 ? NROW : 1)] = wrow[4 * m];
-            } else {
-#pragma unroll
-              for (int m = 0; m < NROW; ++m) rowsub[u][m % (MODE == 1 ? NROW : 1)] = 0u;  // past K: zeros
+            for (int u2 = 0; u2 < 4; ++u2) {
+              if (u2 >= KS) break;
+              const uint32_t k0 = kbase + u2 * TC_BK;  // the lane's chunk lies at k0 + 8 cq
+              const uint32_t nbytes = k0 + 8 * cq < static_cast<uint32_t>(a.D) ? 16u : 0u;  // D: multiple of 8
+              cp_async16(sa + u2 * SUB + dst[t], a.Wp + rowbase[t] + (nbytes ? k0 : 0u) - (nbytes ? 0u : 8u * cq),
+                         nbytes);
             }
           }
         }
+        cp_async_arrive(&ctl.full[s]);
+        if (tma_lane) {
+          if (waited) {
+            issue_x(issued);
+            x_done = issued + 1;
+          } else if (issued + 1 >= static_cast<uint32_t>(STAGES < GU_PRE ? STAGES : GU_PRE)) {
+            pdl_wait();  // x of this step is complete once the previous kernel is
+            waited = true;
+            for (uint32_t i = x_done; i <= issued; ++i) issue_x(i);
+            x_done = issued + 1;
+          }
+        }
+        ++issued;
+      }
+    }
+    // x boxes still owed (a CTA with fewer stages than the ring); every copy this warp started
+    // must land before the CTA can exit
+    if (tma_lane && ok) {
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+      for (uint32_t i = x_done; i < issued; ++i) issue_x(i);
+      x_done = issued;
+    }
+    cp_async_wait_all();
+    if (tma_lane) {
+      const uint32_t lo = x_done > static_cast<uint32_t>(STAGES) ? x_done - STAGES : 0;
+      for (uint32_t i = lo; i < x_done; ++i) {
+        volatile int never = 0;
+        if (!mbar_wait_bounded(&ctl.full[i % STAGES], (i / STAGES) & 1u, TC_DRAIN_NS, &never)) fail();
+      }
+    }
+    __syncwarp();
+  } else if (warp == TC_MMA_WARP) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (one thread)
+      const uint32_t idesc = idesc_bf16_f32(TC_BM, NP, false, false);
+      uint32_t consumed = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = w; u < U && ok; u += W, ++it) {
+        const int buf = it & 1;
+        if (!mbar_wait_bounded(&ctl.tempty[buf], ((it >> 1) & 1) ^ 1, a.wait_ns, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * TC_HALF;
+        for (int sbk = 0; sbk < KBS; ++sbk) {
+          const int s = static_cast<int>(consumed % static_cast<uint32_t>(STAGES));
+          const uint32_t ph = (consumed / static_cast<uint32_t>(STAGES)) & 1u;
+          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          fence_proxy_async();
+          tc_fence_after();
+          for (int u2 = 0; u2 < KS; ++u2) {
+            const uint32_t sg = smem_u32(smem + s * STAGE) + u2 * SUB;
+            const uint32_t sx = sg + AROWS * 128;
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k) {
+              const uint32_t acc = (sbk > 0 || u2 > 0 || k > 0) ? 1u : 0u;
+              umma_f16(d_tmem, smem_desc_sw128(sg + 32u * k, 16u, 1024u), smem_desc_sw128(sx + 32u * k, 16u, 1024u),
+                       idesc, acc);
+            }
+          }
+          umma_commit(&ctl.empty[s]);
+          ++consumed;
+        }
+        if (!ok) break;
+        umma_commit(&ctl.tfull[buf]);
+      }
+      // all MMAs issued by this thread must finish before TMEM is freed
+      umma_commit(&ctl.drain);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(&ctl.drain, 0, TC_DRAIN_NS, &never)) fail();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 9..12)
+    pdl_wait();  // z, scores and the z planes may still be read by the previous step's kernels
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const int half = lane >> 4;
+    const int j = 16 * q + (lane & 15);  // position within the unit; lanes 0-15 gate, 16-31 up
+    const int et = threadIdx.x - 32 * TC_EPI0;  // 0..127
+    constexpr int NH = NP / 2;                  // tokens per lane after the pairing
+    const int b0 = half * NH;
+    int it = 0;
+    for (int u = w; u < U; u += W, ++it) {
+      const int buf = it & 1;
+      const int lo = unit_lo(u), hi = unit_lo(u + 1);
+      const int p = lo + j;
+      const bool valid = p < hi;
+      const bool cand = valid && p < a.nC;
+      // the candidates' down-column norms, fetched while the accumulators are still being built
+      float n2v = 0.f;
+      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldg(a.rc + p), a.N, a.err));
+      if (et == 0)
+        ctl.seg_ok[buf] = mbar_wait_bounded(&ctl.tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
+      epi_bar();
+      if (!ctl.seg_ok[buf]) {
+        if (et == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf) * TC_HALF;
+      float acc[NP];
+#pragma unroll
+      for (int c = 0; c < NP; c += 16) {
+        uint32_t t16[16];
+        tmem_ld16(taddr + c, t16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(t16[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
+      // pair gate (lanes 0-15) with up (lanes 16-31) of the same position: lane l < 16 takes
+      // tokens [0, NP/2), lane l + 16 tokens [NP/2, NP)
+      float zz[NH];
+#pragma unroll
+      for (int i = 0; i < NH; ++i) {
+        const float mine = half ? acc[i] : acc[NH + i];
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+        const float g = half ? other : acc[i];
+        const float uu = half ? acc[NH + i] : other;
+        zz[i] = silu_t(g) * uu;
+      }
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < NH; ++i)
+        if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      if (cand) {
+        float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc + b0);
+#pragma unroll
+        for (int i4 = 0; i4 < NH / 4; ++i4)
+          if (b0 + 4 * i4 < a.ldzc) dst[i4] = make_float4(zz[4 * i4], zz[4 * i4 + 1], zz[4 * i4 + 2], zz[4 * i4 + 3]);
+        if (half == 0) a.scores[p] = m * n2v;
+      } else if (valid) {
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+          if (b0 + i < a.B) {
+            uint16_t h16, l16;
+            split_bf16(zz[i], h16, l16);
+            const size_t o = static_cast<size_t>(b0 + i) * a.ldk + (p - a.nC);
+            a.zk[o] = h16;
+            a.zk_lo[o] = l16;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == TC_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TC_TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ selection + down over R u S
+template <int NP>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant__ DownTcArgs a) {
+  using Cfg = DnCfg<NP>;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr uint32_t STAGE_BYTES = Cfg::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ TcCtl ctl;
+  __shared__ RadixScratch<TC_PROD_THREADS> rsc;
+  __shared__ int dwin[DN_WIN_WORDS];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int SK = a.split;
+  const uint32_t rank = SK > 1 ? cluster_rank() : 0u;
+  const int ci = static_cast<int>(blockIdx.x) / SK;  // cluster index
+
+  if (a.sel && ci == 0) {
+    // ------------------------------------------------------------ the selecting cluster
+    if (rank == 0) {
+      pdl_wait();  // this step's scores and z; S, memory, step and the z planes of the previous step
+      pdl_trigger();
+      down_select(a, smem, rsc);
+    }
+    return;
+  }
+
+  volatile int* abort_flag = &ctl.abort_flag;
+  volatile unsigned* sel_seen = &ctl.sel_seen;
+  const int unit0 = ci - a.sel, nunits = static_cast<int>(gridDim.x) / SK - a.sel;
+  const int U = a.units;
+  const int G = a.D / 8;  // output groups of 8 (16 bytes); a unit is a range of whole groups
+  auto unit_lo = [&](int u) { return 8 * static_cast<int>(static_cast<long long>(u) * G / U); };
+  // this CTA's k-blocks: R blocks [r0, r1), then selected blocks [s0, s1) (block kbr + t holds
+  // selected items 64 t ..)
+  const int kbs = (a.k + TC_BK - 1) / TC_BK;
+  const int r0 = static_cast<int>(rank) * a.kbr / SK, r1 = (static_cast<int>(rank) + 1) * a.kbr / SK;
+  const int s0 = static_cast<int>(rank) * kbs / SK, s1 = (static_cast<int>(rank) + 1) * kbs / SK;
+  const int nblk = (r1 - r0) + (s1 - s0);  // stages per unit
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl.full[s], TC_PROD_THREADS);
+      mbar_init(&ctl.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl.tfull[b], 1);
+      mbar_init(&ctl.tempty[b], 4);
+    }
+    mbar_init(&ctl.drain, 1);
+    ctl.abort_flag = 0;
+    ctl.sel_seen = a.epoch - 1u;
+    fence_mbar_init();
+  }
+  if (warp == TC_MMA_WARP) {
+    tmem_alloc(&ctl.tmem_base, TC_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  pdl_trigger();
+  // Only the producers touch this step's data before the epilogue (which follows their copies
+  // through the barriers); they wait for the previous kernel before the z planes (see below).
+
+  auto fail = [&]() {
+    if (!*abort_flag) {
+      *abort_flag = 1;
+      atomicOr(a.err, DEVERR_TIMEOUT_DECODE_TC);
+    }
+  };
+
+  if (warp < TC_PW) {
+    // ------------------------------------------------------------ producers (eight warps)
+    // Per stage: the A pieces (item i, output half h) p = 2 i + h are copied by lane group
+    // grp = p % 32 (16 contiguous bytes per lane, 8 lanes per 128-byte piece), so a warp reads two
+    // items' 256 contiguous bytes; the z-plane chunks (NP / 16 per lane) follow. Items past the end
+    // of R or of S are zero-filled, as are token rows past B. Each warp keeps the channels of its
+    // items for DN_WIN stages in shared memory, fetched together (one round of loads per window).
+    // The down columns and the channels of R are constant between partitions, so the A copies of
+    // the first stages go out before griddepcontrol.wait; their z planes follow it.
+    const int cq = lane & 7, grp = (warp * 32 + lane) >> 3;
+    const int pt = warp * 32 + lane;
+    const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(a.D);
+    const size_t row3 = 3 * static_cast<size_t>(a.D);
+    const uint16_t* zk_lo = a.zk + a.zk_lo_off;
+    const int h = grp & 1, ip = (grp & 3) >> 1;  // output half; item parity within the warp's pair
+    const int nrs = r1 - r0;                     // R stages of each unit
+    int* mywin = dwin + warp * (DN_WIN * 8);
+    int wlo = 0, whi = 0;                        // stages [wlo, whi) are in the window
+    auto fill = [&](int bi0) {
+      const int seg_end = bi0 < nrs ? nrs : nblk;
+      wlo = bi0;
+      whi = min(seg_end, bi0 + DN_WIN);
+      int c[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int x = lane + 32 * v;
+        const int bj = wlo + (x >> 3), e = x & 7;
+        const int i = 2 * warp + (e & 1) + 16 * (e >> 1);  // item within its k-block
+        c[v] = -1;
+        if (bj < whi) {
+          if (bj < nrs) {
+            const int item = (r0 + bj) * TC_BK + i;
+            if (item < a.nR) c[v] = __ldg(a.ch_r + item);
+          } else {
+            const int item = (s0 + bj - nrs) * TC_BK + i;
+            if (item < a.k) c[v] = __ldcg(a.ch_s + item);
+          }
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int v = 0; v < 8; ++v) mywin[lane + 32 * v] = c[v];
+      __syncwarp();
+    };
+    auto issue_a = [&](int bi, uint32_t sa, int d0, bool dok) {
+      if (!dok) return;  // outputs past the unit's end are left unwritten (their rows are never read)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = (grp >> 1) + 16 * t;
+        int ch = mywin[(bi - wlo) * 8 + ip + 2 * t];
+        const uint32_t nb = ch >= 0 ? 16u : 0u;
+        if (ch >= 0) ch = guard_ch(ch, a.N, a.err);
+        cp_async16(sa + h * (TC_BK * 128) + i * 128 + ((cq ^ (i & 7)) << 4),
+                   W2 + (nb ? static_cast<size_t>(ch) * row3 + d0 : 0), nb);
+      }
+    };
+    auto issue_b = [&](int bi, uint32_t sa) {
+      const int kb = bi < nrs ? r0 + bi : a.kbr + s0 + (bi - nrs);  // column block of the z planes
+      // chunk c = pt + 256 v -> plane c / (8 NP), token row (c / 8) % NP, chunk c % 8
+#pragma unroll
+      for (int v = 0; v < NP / 16; ++v) {
+        const int c = pt + TC_PROD_THREADS * v;
+        const int plane = c / (8 * NP), b = (c >> 3) % NP, zq = c & 7;
+        const uint32_t nb = b < a.B ? 16u : 0u;
+        const uint16_t* zsrc = (plane ? zk_lo : a.zk) + static_cast<size_t>(b) * a.ldk + kb * TC_BK + 8 * zq;
+        cp_async16(sa + Cfg::A_BYTES + plane * (NP * 128) + b * 128 + ((zq ^ (b & 7)) << 4), nb ? zsrc : a.zk, nb);
+      }
+    };
+    // stages whose A copies go out before the wait: the first DN_PRE R stages of the first unit (more
+    // only queue behind the memory system's back-pressure and hold the z planes, and so the MMAs, back)
+    const int pre = unit0 < U ? min(DN_PRE, min(STAGES, nrs)) : 0;
+    if (pre == 0) pdl_wait();
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int unit = unit0; unit < U && ok; unit += nunits) {
+      const int lo = unit_lo(unit), hi = unit_lo(unit + 1);
+      const int d0 = lo + 64 * h + 8 * cq;
+      const bool dok = d0 < hi;
+      for (int bi = 0; bi < nblk; ++bi) {
+        if (bi == nrs && bi < nblk) {
+          // first selected block: the selection of this step must be complete. Warp 0 polls the
+          // flag in global memory and posts what it saw in shared memory; the other warps watch
+          // that (every wait bounded; no barrier across warps that a warp which gave up earlier
+          // would miss).
+          int good = 1;
+          if (lane == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            if (warp == 0) {
+              while (static_cast<int>(ld_acquire_u32(a.flag) - a.epoch) < 0) {
+                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+                  good = 0;
+                  break;
+                }
+                __nanosleep(256);
+              }
+              if (good) {
+                __threadfence_block();
+                *sel_seen = a.epoch;
+              }
+            } else {
+              while (static_cast<int>(*sel_seen - a.epoch) < 0) {
+                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+                  good = 0;
+                  break;
+                }
+                __nanosleep(64);
+              }
+              if (good) (void)ld_acquire_u32(a.flag);  // acquire for this warp's own reads
+            }
+            if (!good) fail();
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          __syncwarp();  // orders lane 0's acquire before the other lanes' reads of the selection
+          if (!good) {
+            ok = false;
+            break;
+          }
+        }
+        if (bi < wlo || bi >= whi) fill(bi);
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1u;
         bool got = true;
         if (lane == 0) {
-          got = mbar_wait_bounded(&ctl->empty[s], ph ^ 1u, a.wait_ns, abort_flag);
+          got = mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, a.wait_ns, abort_flag);
           if (!got) fail();
-          else if (warp == 0) mbar_arrive_expect_tx(&ctl->full[s], tx_bytes);
         }
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
@@ -295,218 +782,122 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           break;
         }
         const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        if (MODE == 0) {
-          // row by row, both k-blocks: KSUB x 128 contiguous bytes of each row back to back
-#pragma unroll
-          for (int m = 0; m < NROW; ++m) {
-            const int r = rg + 8 * m;
-#pragma unroll
-            for (int u = 0; u < KSUB; ++u) {
-              const int d0 = (sbk * KSUB + u) * TC_BK + 8 * cq;
-              const uint32_t nbytes = d0 < a.D ? 16u : 0u;  // D is a multiple of 8: chunks all in or out
-              const uint16_t* src = Wbase + rowoff[m] + (nbytes ? d0 : 0);
-              const uint32_t dst = sa + u * Cfg::SUB_BYTES + r * 128 + ((cq ^ (r & 7)) << 4);
-              cp_async16(dst, src, nbytes);
-              cp_async16(dst + TC_BM * 128, src + a.D, nbytes);
+        issue_a(bi, sa, d0, dok);
+        if (issued < static_cast<uint32_t>(pre)) {
+          if (issued + 1 == static_cast<uint32_t>(pre)) {
+            // the z planes of this step exist once the previous kernel has finished
+            pdl_wait();
+            for (int bj = 0; bj < pre; ++bj) {
+              issue_b(bj, smem_u32(smem + bj * STAGE_BYTES));
+              cp_async_arrive(&ctl.full[bj]);
             }
           }
         } else {
-#pragma unroll
-          for (int u = 0; u < KSUB; ++u) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int d0 = tile * TC_BM + 64 * h + 8 * cq;
-              const uint32_t nbytes = d0 < a.D ? 16u : 0u;
-              const uint16_t* base = Wbase + (nbytes ? d0 : 0);
-#pragma unroll
-              for (int m = 0; m < NROW; ++m) {
-                const int r = rg + 8 * m;
-                cp_async16(sa + u * Cfg::SUB_BYTES + h * (TC_BK * 128) + r * 128 + ((cq ^ (r & 7)) << 4),
-                           base + rowsub[u][m % (MODE == 1 ? NROW : 1)], nbytes);
-              }
-            }
-          }
-        }
-        cp_async_commit();
-        if (issued >= static_cast<uint32_t>(LAG)) {
-          cp_async_wait<LAG>();
-          fence_proxy_async();
-          mbar_arrive(&ctl->full[(issued - LAG) % STAGES]);
-        }
-        if (warp == 0 && lane == 0) {
-#pragma unroll
-          for (int u = 0; u < KSUB; ++u) {
-            uint8_t* sb = smem + s * STAGE_BYTES + u * Cfg::SUB_BYTES + Cfg::A_BYTES;
-            const int kx = (sbk * KSUB + u) * TC_BK;  // may lie past K: the box then reads zeros
-            tma_load_2d(sb, &mapB, &ctl->full[s], kx, 0);
-            if (MODE == 1) tma_load_2d(sb + NP * 128, &mapB2, &ctl->full[s], kx, 0);  // z lo plane
-          }
+          issue_b(bi, sa);
+          cp_async_arrive(&ctl.full[s]);
         }
         ++issued;
       }
     }
-    // the last stages' arrivals, and every copy this warp started must land before the CTA can exit
-    cp_async_wait<0>();
-    fence_proxy_async();
-    if (ok)
-      for (uint32_t u = issued > static_cast<uint32_t>(LAG) ? issued - LAG : 0; u < issued; ++u)
-        mbar_arrive(&ctl->full[u % STAGES]);
-    if (warp == 0 && lane == 0) {
-      const uint32_t lo = issued > static_cast<uint32_t>(STAGES) ? issued - STAGES : 0;
-      for (uint32_t u = lo; u < issued; ++u) {
-        volatile int never = 0;
-        if (!mbar_wait_bounded(&ctl->full[u % STAGES], (u / STAGES) & 1u, TC_DRAIN_NS, &never)) fail();
-      }
-    }
+    // an abort before the wait still owes the z planes of the first stages nothing: their barriers
+    // are only drained below through the copies of this warp
+    if (issued < static_cast<uint32_t>(pre)) pdl_wait();
+    if (!a.sel && a.count_step && blockIdx.x == 0 && threadIdx.x == 0) *a.step += 1;
+    // every copy this warp started must land before the CTA can exit
+    cp_async_wait_all();
     __syncwarp();
   } else if (warp == TC_MMA_WARP) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
-      const uint32_t idesc = idesc_bf16_f32(TC_BM, MODE == 0 ? NP : 2 * NP, false, MODE == 1);
+      const uint32_t idesc = idesc_bf16_f32(TC_BM, 2 * NP, false, true);
       uint32_t consumed = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = unit; tile < tiles && ok; tile += nunits, ++it) {
+      for (int unit = unit0; unit < U && ok; unit += nunits, ++it) {
         const int buf = it & 1;
-        if (!mbar_wait_bounded(&ctl->tempty[buf], ((it >> 1) & 1) ^ 1, a.wait_ns, abort_flag)) {
+        if (!mbar_wait_bounded(&ctl.tempty[buf], ((it >> 1) & 1) ^ 1, a.wait_ns, abort_flag)) {
           fail();
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * HALF_COLS;
-        for (int sbk = sb_lo; sbk < sb_hi; ++sbk) {
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * TC_HALF;
+        for (int bi = 0; bi < nblk; ++bi) {
           const int s = consumed % STAGES;
           const uint32_t ph = (consumed / STAGES) & 1u;
-          if (!mbar_wait_bounded(&ctl->full[s], ph, a.wait_ns, abort_flag)) {
+          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag)) {
             fail();
             ok = false;
             break;
           }
+          fence_proxy_async();
           tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
-          for (int u = 0; u < KSUB; ++u) {
-            const uint32_t sa = smem_u32(smem + s * STAGE_BYTES) + u * Cfg::SUB_BYTES;
-            const uint32_t sb = sa + Cfg::A_BYTES;
-#pragma unroll
-            for (int k = 0; k < TC_BK / 16; ++k) {
-              const uint32_t acc = (sbk > sb_lo || u > 0 || k > 0) ? 1u : 0u;
-              const uint64_t bdesc = smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-              if (MODE == 0) {
-                umma_f16(d_tmem, smem_desc_sw128(sa + 32u * k, 16u, 1024u), bdesc, idesc, acc);
-                umma_f16(d_tmem + static_cast<uint32_t>(NP),
-                         smem_desc_sw128(sa + TC_BM * 128 + 32u * k, 16u, 1024u), bdesc, idesc, acc);
-              } else {
-                umma_f16(d_tmem, smem_desc_sw128(sa + 2048u * k, TC_BK * 128, 1024u), bdesc, idesc, acc);
-              }
-            }
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            const uint32_t acc = (bi > 0 || k > 0) ? 1u : 0u;
+            umma_f16(d_tmem, smem_desc_sw128(sa + 2048u * k, TC_BK * 128, 1024u),
+                     smem_desc_sw128(sb + 32u * k, 16u, 1024u), idesc, acc);
           }
-          umma_commit(&ctl->empty[s]);
+          umma_commit(&ctl.empty[s]);
           ++consumed;
         }
         if (!ok) break;
-        umma_commit(&ctl->tfull[buf]);
+        umma_commit(&ctl.tfull[buf]);
       }
-      // all MMAs issued by this thread must finish before TMEM is freed
-      umma_commit(&ctl->drain);
+      umma_commit(&ctl.drain);
       volatile int never = 0;
-      if (!mbar_wait_bounded(&ctl->drain, 0, TC_DRAIN_NS, &never)) fail();
+      if (!mbar_wait_bounded(&ctl.drain, 0, TC_DRAIN_NS, &never)) fail();
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 3..6)
-    const int q = warp & 3;  // TMEM lane quarter of this warp
+    // ------------------------------------------------------------ epilogue (warps 9..12)
+    const int q = warp & 3;
     const int r = 32 * q + lane;
-    const int et = threadIdx.x - 32 * (TC_MMA_WARP + 1);  // 0..127
-    // split tiles: the norm of the candidate row this thread finishes after the cluster exchange,
-    // fetched now while the tile streams
-    if (MODE == 0 && SK > 1 && unit < tiles) {
-      const int p = unit * TC_BM + static_cast<int>(rank) * (TC_BM / SK) + et / SK;
-      if (p < a.nC) ctl->n2s[et] = a.n2[guard_ch(a.rc[p], a.N, a.err)];
-    }
+    const int et = threadIdx.x - 32 * TC_EPI0;
     int it = 0;
-    for (int tile = unit; tile < tiles; tile += nunits, ++it) {
+    for (int unit = unit0; unit < U; unit += nunits, ++it) {
       const int buf = it & 1;
-      // the candidates' down-column norms, fetched while the accumulators are still being built
-      float n2v = 0.f;
-      if (MODE == 0 && SK == 1) {
-        const int p = tile * TC_BM + r;
-        if (p < a.nC) n2v = a.n2[guard_ch(a.rc[p], a.N, a.err)];
-      }
       if (et == 0)
-        ctl->seg_ok[it & 1] = mbar_wait_bounded(&ctl->tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
+        ctl.seg_ok[buf] = mbar_wait_bounded(&ctl.tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
       epi_bar();
-      if (!ctl->seg_ok[it & 1]) {
+      if (!ctl.seg_ok[buf]) {
         if (et == 0) fail();
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf) * HALF_COLS;
-      // tokens 0..NP-1 of the accumulator halves: gate and up (gate/up), or the z hi and lo parts (down)
-      float gv[NP], uv[NP];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf) * TC_HALF;
+      // tokens 0..NP-1 of the z hi and lo halves of the accumulator
+      float yv[NP];
 #pragma unroll
       for (int c = 0; c < NP; c += 16) {
-        uint32_t t16[16];
+        uint32_t t16[16], l16[16];
         tmem_ld16(taddr + c, t16);
+        tmem_ld16(taddr + NP + c, l16);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) gv[c + j] = __uint_as_float(t16[j]);
-        tmem_ld16(taddr + NP + c, t16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) uv[c + j] = __uint_as_float(t16[j]);
+        for (int i = 0; i < 16; ++i) yv[c + i] = __uint_as_float(t16[i]) + __uint_as_float(l16[i]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
-
+      if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
       if (SK > 1) {
-        // partial of a split tile: to this CTA's shared memory (the stage ring, idle by now: all
-        // copies landed and all MMAs finished), rows of PCOLS floats
-        float* pb = reinterpret_cast<float*>(smem) + r * Cfg::PCOLS;
+        // partial of a split unit: to this CTA's shared memory (the stage ring, idle by now: all
+        // copies landed and all MMAs finished), rows of NP floats
+        float* pb = reinterpret_cast<float*>(smem) + r * NP;
 #pragma unroll
-        for (int c = 0; c < NP; ++c) {
-          if (MODE == 0) {
-            pb[c] = gv[c];
-            pb[NP + c] = uv[c];
-          } else {
-            pb[c] = gv[c] + uv[c];
-          }
-        }
+        for (int c = 0; c < NP; ++c) pb[c] = yv[c];
         continue;
       }
-      if (MODE == 0) {
-        const int p = tile * TC_BM + r;
-        if (p < a.rows) {
-          float m = 0.f;
+      const int d = unit_lo(unit) + r;
+      if (d < unit_lo(unit + 1)) {
 #pragma unroll
-          for (int b = 0; b < NP; ++b) {
-            if (b < a.B) {
-              const float zz = silu_t(gv[b]) * uv[b];
-              a.z[static_cast<size_t>(b) * a.ldz + p] = zz;
-              if (p >= a.nC) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
-                const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
-                a.zk[o] = *reinterpret_cast<const uint16_t*>(&hi);
-                a.zk_lo[o] = *reinterpret_cast<const uint16_t*>(&lo);
-              }
-              m = fmaxf(m, fabsf(zz));
-            }
-          }
-          if (p < a.nC) a.scores[p] = m * n2v;
-        }
-      } else {
-        const int d = tile * TC_BM + r;
-        if (d < a.rows) {
-#pragma unroll
-          for (int b = 0; b < NP; ++b) {
-            if (b < a.B) {
-              const float yv = gv[b] + uv[b];
-              if (a.out_f32)
-                static_cast<float*>(a.y)[static_cast<size_t>(b) * a.rows + d] = yv;
-              else
-                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.rows + d] = __float2bfloat16_rn(yv);
-            }
+        for (int b = 0; b < NP; ++b) {
+          if (b < a.B) {
+            if (a.out_f32)
+              static_cast<float*>(a.y)[static_cast<size_t>(b) * a.D + d] = yv[b];
+            else
+              static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.D + d] = __float2bfloat16_rn(yv[b]);
           }
         }
       }
@@ -514,80 +905,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 
   if (SK > 1) {
-    // ------------------------------------------------------------ cluster reduction of the split tile
+    // ------------------------------------------------------------ cluster reduction of the split unit
     // Every thread of the cluster passes both barriers. Between them, epilogue thread et of rank
     // `rank` finishes row rank * 128 / SK + et / SK for tokens [part * NP / SK, (part + 1) * NP / SK),
     // part = et % SK, adding the SK partials in rank order.
     cluster_sync_all();
-    if (warp > TC_MMA_WARP && unit < tiles && !*abort_flag) {
-      const int et = threadIdx.x - 32 * (TC_MMA_WARP + 1);
+    if (warp >= TC_EPI0 && unit0 < U && !*abort_flag) {
+      const int et = threadIdx.x - 32 * TC_EPI0;
       const int rows_per = TC_BM / SK, tpt = NP / SK;
       const int rl = et / SK, part = et % SK;
       const int row = static_cast<int>(rank) * rows_per + rl;
       const int b0 = part * tpt;
-      const uint32_t pbase = smem_u32(smem) + static_cast<uint32_t>(row * Cfg::PCOLS) * 4u;
-      float m = 0.f;
-      const int p = unit * TC_BM + row;
-      const float n2v = MODE == 0 && p < a.nC ? ctl->n2s[et] : 0.f;
+      const int d = unit_lo(unit0) + row;
+      const bool dok = d < unit_lo(unit0 + 1);
+      const uint32_t pbase = smem_u32(smem) + static_cast<uint32_t>(row * NP) * 4u;
       uint32_t peer[8];
 #pragma unroll
       for (int pr = 0; pr < 8; ++pr) peer[pr] = pr < SK ? map_peer(pbase, static_cast<uint32_t>(pr)) : 0u;
       // tokens two at a time (tpt = NP / SK is even): SK peers x 8-byte loads, added in rank order
 #pragma unroll 2
-      for (int j = 0; j < tpt; j += 2) {
-        const int b = b0 + j;
-        float2 g2 = make_float2(0.f, 0.f), u2 = make_float2(0.f, 0.f);
-        float2 lg[8], lu[8];
+      for (int jj = 0; jj < tpt; jj += 2) {
+        const int b = b0 + jj;
+        float2 lg[8];
 #pragma unroll
-        for (int pr = 0; pr < 8; ++pr) {
-          if (pr < SK) {
-            lg[pr] = ld_peer2(peer[pr] + 4u * b);
-            if (MODE == 0) lu[pr] = ld_peer2(peer[pr] + 4u * (NP + b));
-          }
-        }
+        for (int pr = 0; pr < 8; ++pr)
+          if (pr < SK) lg[pr] = ld_peer2(peer[pr] + 4u * b);
+        float2 g2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int pr = 0; pr < 8; ++pr) {
           if (pr < SK) {
             g2.x += lg[pr].x;
             g2.y += lg[pr].y;
-            if (MODE == 0) {
-              u2.x += lu[pr].x;
-              u2.y += lu[pr].y;
+          }
+        }
+        if (dok) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int bb = b + hh;
+            const float g = hh ? g2.y : g2.x;
+            if (bb < a.B) {
+              if (a.out_f32)
+                static_cast<float*>(a.y)[static_cast<size_t>(bb) * a.D + d] = g;
+              else
+                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(bb) * a.D + d] = __float2bfloat16_rn(g);
             }
           }
         }
-        for (int h = 0; h < 2; ++h) {
-        const int b = b0 + j + h;
-        const float g = h ? g2.y : g2.x, u = h ? u2.y : u2.x;
-        if (b >= a.B) continue;
-        if (MODE == 0) {
-          if (p < a.rows) {
-            const float zz = silu_t(g) * u;
-            a.z[static_cast<size_t>(b) * a.ldz + p] = zz;
-            if (p >= a.nC) {
-              const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
-              const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
-              const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
-              a.zk[o] = *reinterpret_cast<const uint16_t*>(&hi);
-              a.zk_lo[o] = *reinterpret_cast<const uint16_t*>(&lo);
-            }
-            m = fmaxf(m, fabsf(zz));
-          }
-        } else {
-          const int d = unit * TC_BM + row;
-          if (d < a.rows) {
-            if (a.out_f32)
-              static_cast<float*>(a.y)[static_cast<size_t>(b) * a.rows + d] = g;
-            else
-              static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(b) * a.rows + d] = __float2bfloat16_rn(g);
-          }
-        }
-        }
-      }
-      if (MODE == 0) {
-        // the row's SK threads are adjacent lanes: combine their maxima
-        for (int o = SK / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (part == 0 && p < a.nC) a.scores[p] = m * n2v;
       }
     }
     cluster_sync_all();  // no CTA leaves while a peer may still read its partials
@@ -597,27 +960,107 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   if (warp == TC_MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem_base, TC_TMEM_COLS);
   }
 }
 
 // ------------------------------------------------------------------ launchers
-template <int MODE, int NP>
-static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, DecodeTcArgs args, int num_sms,
-                                cudaStream_t st) {
-  constexpr size_t smem = tc_smem_bytes<MODE, NP>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode_tc<MODE, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = true;
+namespace {
+// The gate/up work split: one CTA per SM, `units` ragged row ranges of at most 64 positions,
+// rows_cap = their largest size rounded up to 16. A stage holds KS k-blocks, the most (up to 4) that
+// leave three stages: longer runs per gathered row were measured to matter more than ring depth.
+// Past the ring lies room for the MMA's reads of the unwritten rows of the last sub-stage (128
+// rows of 128 bytes from its A tile, less what the sub-stage itself holds).
+struct GuSplit {
+  int grid, units, rows_cap, ks, stages;
+  size_t smem;
+};
+GuSplit gateup_split(int P, int NP, int num_sms) {
+  GuSplit g{};
+  const int W = num_sms > 0 ? num_sms : 1;
+  const long long m =
+      P > 0 ? (P + static_cast<long long>(GU_MAX_ROWS) * W - 1) / (static_cast<long long>(GU_MAX_ROWS) * W) : 1;
+  g.units = static_cast<int>(m * W);
+  g.grid = W;
+  const long long rows = P > 0 ? (P + g.units - 1) / g.units : 1;
+  g.rows_cap = static_cast<int>((rows + 15) / 16 * 16);
+  const uint32_t sub = static_cast<uint32_t>(2 * g.rows_cap + NP) * 128u;
+  const uint32_t slack = sub >= TC_BM * 128u ? 0u : TC_BM * 128u - sub;
+  const uint32_t budget = 227u * 1024u - 1024u - static_cast<uint32_t>(sizeof(TcCtl)) - 64u - slack;
+  // KS = the most k-blocks per stage (at most 4) that still leaves three stages
+  g.ks = 1;
+  for (int ks = 4; ks >= 1; --ks) {
+    if (budget / (ks * sub) >= 3) {
+      g.ks = ks;
+      break;
+    }
   }
-  const int tiles = (args.rows + TC_BM - 1) / TC_BM;
-  const int KB = (args.K + TC_BK - 1) / TC_BK;
-  constexpr int KSUB = TcCfg<MODE, NP>::KS;
-  const int KBS = (KB + KSUB - 1) / KSUB;
-  if (tiles <= 0 || KB <= 0) return cudaSuccess;
+  const int st = static_cast<int>(budget / (g.ks * sub));
+  g.stages = st > TC_MAX_STAGES ? TC_MAX_STAGES : (st < 2 ? 2 : st);
+  g.smem = 1024 + static_cast<size_t>(g.stages) * g.ks * sub + slack;
+  return g;
+}
+
+template <int NP>
+cudaError_t launch_gateup_np(const CUtensorMap& xm, GateUpTcArgs a, int num_sms, cudaStream_t st) {
+  const int P = a.nC + a.nR;
+  if (P <= 0) return cudaSuccess;
+  const GuSplit g = gateup_split(P, NP, num_sms);
+  static size_t configured = 0;
+  if (g.smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_gateup_tc<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(g.smem));
+    if (e != cudaSuccess) return e;
+    configured = g.smem;
+  }
+  a.units = g.units;
+  a.rows_cap = g.rows_cap;
+  a.ks = g.ks;
+  a.stages = g.stages;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(g.grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = g.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gateup_tc<NP>, xm, a);
+}
+
+// The down work split: a cluster of `split` CTAs per unit of at most 128 outputs (whole groups of
+// 8), plus the selecting cluster first. Among splits 1, 2, 4, 8 (each at most the k-blocks of the
+// shorter of R and S, or of R alone) take the one whose busiest CTA streams the fewest
+// rows x k-blocks, with units of at least 64 outputs where possible (shorter runs per gathered
+// column cost DRAM efficiency); ties go to the smaller split.
+template <int NP>
+cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
+  // the ring, or the selecting CTA's keys (|C| of them) if those need more
+  size_t smem = dn_smem_bytes<NP>();
+  constexpr size_t kStatic = sizeof(TcCtl) + sizeof(RadixScratch<TC_PROD_THREADS>) + sizeof(int) * DN_WIN_WORDS + 64;
+  constexpr size_t kMaxDyn = 227 * 1024 - kStatic;
+  const size_t c16 = (static_cast<size_t>(a.nC) * 4 + 15) & ~size_t(15);
+  const size_t keys_bytes = 1024 + c16;
+  const size_t small_bytes = keys_bytes + 2 * c16 + ((static_cast<size_t>(a.k) * 4 + 15) & ~size_t(15));
+  const size_t z_bytes = small_bytes + static_cast<size_t>(a.nC) * a.ldzc * 4;
+  if (a.sel) {
+    if (keys_bytes > kMaxDyn) return cudaErrorInvalidValue;  // |C| beyond what one CTA's keys can hold
+    const size_t want = z_bytes <= kMaxDyn ? z_bytes : (small_bytes <= kMaxDyn ? small_bytes : keys_bytes);
+    if (want > smem) smem = want;
+  }
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k_down_tc<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  const int G = a.D / 8;
+  const int tiles = (a.D + TC_BM - 1) / TC_BM;
+  const int kbs = (a.k + TC_BK - 1) / TC_BK;
+  const int KBT = a.kbr + kbs;
   cudaLaunchConfig_t cfg{};
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = smem;
@@ -627,48 +1070,114 @@ static cudaError_t launch_tc_np(const CUtensorMap& b, const CUtensorMap& b2, Dec
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   cfg.attrs = attr;
-  // split: the largest power of two <= 8 such that tiles x split CTAs fit the SMs at once (one CTA
-  // per SM) with at least one k-block per CTA, confirmed by the cluster occupancy query
-  int split = 1;
-  while (split < 8 && tiles * split * 2 <= num_sms && split * 2 <= KBS) split *= 2;
-  for (; split > 1; split /= 2) {
-    attr[1].val.clusterDim.x = split;
+  const int sel = a.sel ? 1 : 0;
+  if (KBT <= 0 || G <= 0) {
+    // nothing to stream: the selection (or the step count) only
+    if (!sel && !a.count_step) return cudaSuccess;
+    a.split = 1;
+    a.units = 0;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(1);
+    return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, a);
+  }
+  // The split depends only on these sizes and the device: computed once per shape (the occupancy
+  // queries cost host time on every step otherwise).
+  struct Key {
+    int D, kbr, kbs, sel, sms, dev;
+  };
+  struct Entry {
+    Key key;
+    int sk, u;
+  };
+  static Entry cache[8];
+  static int cache_n = 0;
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  const Key key{a.D, a.kbr, kbs, sel, num_sms, dev};
+  int best_sk = 1, best_u = tiles;
+  bool hit = false;
+  for (int i = 0; i < cache_n; ++i) {
+    const Key& c = cache[i].key;
+    if (c.D == key.D && c.kbr == key.kbr && c.kbs == key.kbs && c.sel == key.sel && c.sms == key.sms && c.dev == key.dev) {
+      best_sk = cache[i].sk;
+      best_u = cache[i].u;
+      hit = true;
+      break;
+    }
+  }
+  const int minblk = a.kbr > 0 && kbs > 0 ? (a.kbr < kbs ? a.kbr : kbs) : KBT;
+  const int u64 = G / 8 > 0 ? G / 8 : 1;  // units of >= 64 outputs
+  long long best_cost = -1;
+  for (int sk = 1; sk <= 8 && !hit; sk *= 2) {
+    if (sk > 1 && sk > minblk) break;
+    int ncl = num_sms;
+    if (sk > 1) {
+      attr[1].val.clusterDim.x = sk;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
+      cfg.gridDim = dim3(sk * (num_sms / sk));
+      ncl = 0;
+      if (cudaOccupancyMaxActiveClusters(&ncl, k_down_tc<NP>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        continue;
+      }
+      ncl -= sel;
+      if (ncl < tiles) continue;  // a split unit must have its own cluster, all resident at once
+    } else {
+      ncl -= sel;
+    }
+    if (ncl < 1) continue;
+    int U = ncl < u64 ? ncl : u64;
+    if (U < tiles) U = tiles;
+    const long long rows = 8LL * ((G + U - 1) / U);
+    const long long rounds = (U + ncl - 1) / ncl;
+    const long long blk = (a.kbr + sk - 1) / sk + (kbs + sk - 1) / sk;
+    const long long cost = rounds * rows * blk;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_sk = sk;
+      best_u = U;
+    }
+  }
+  if (!hit) {
+    cache[cache_n < 8 ? cache_n++ : 7] = Entry{key, best_sk, best_u};
+  }
+  a.split = best_sk;
+  a.units = best_u;
+  if (best_sk > 1) {
+    attr[1].val.clusterDim.x = best_sk;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
-    cfg.gridDim = dim3(tiles * split);
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, k_decode_tc<MODE, NP>, &cfg) == cudaSuccess && clusters >= tiles)
-      break;
-    (void)cudaGetLastError();
-  }
-  args.split = split;
-  if (split == 1) {
+    cfg.gridDim = dim3((best_u + sel) * best_sk);
+  } else {
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
+    const int ctas = best_u < num_sms - sel ? best_u : num_sms - sel;
+    cfg.gridDim = dim3((ctas > 0 ? ctas : 1) + sel);
   }
-  return cudaLaunchKernelEx(&cfg, k_decode_tc<MODE, NP>, b, b2, args);
+  return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, a);
 }
+}  // namespace
 
-template <int MODE>
-static cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& b2, const DecodeTcArgs& args, int num_sms,
-                             cudaStream_t st) {
+cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int num_sms, cudaStream_t st) {
   switch (args.NP) {
-    case 16: return launch_tc_np<MODE, 16>(b, b2, args, num_sms, st);
-    case 32: return launch_tc_np<MODE, 32>(b, b2, args, num_sms, st);
-    case 48: return launch_tc_np<MODE, 48>(b, b2, args, num_sms, st);
-    case 64: return launch_tc_np<MODE, 64>(b, b2, args, num_sms, st);
+    case 16: return launch_gateup_np<16>(x_map, args, num_sms, st);
+    case 32: return launch_gateup_np<32>(x_map, args, num_sms, st);
+    case 48: return launch_gateup_np<48>(x_map, args, num_sms, st);
+    case 64: return launch_gateup_np<64>(x_map, args, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gateup_tc(const CUtensorMap& x_map, const DecodeTcArgs& args, int num_sms, cudaStream_t st) {
-  return launch_tc<0>(x_map, x_map, args, num_sms, st);
-}
-
-cudaError_t launch_down_tc(const CUtensorMap& zk_map, const CUtensorMap& zk_lo_map, const DecodeTcArgs& args,
-                           int num_sms, cudaStream_t st) {
-  return launch_tc<1>(zk_map, zk_lo_map, args, num_sms, st);
+cudaError_t launch_down_tc(DownTcArgs args, int num_sms, cudaStream_t st) {
+  switch (args.NP) {
+    case 16: return launch_down_np<16>(args, num_sms, st);
+    case 32: return launch_down_np<32>(args, num_sms, st);
+    case 48: return launch_down_np<48>(args, num_sms, st);
+    case 64: return launch_down_np<64>(args, num_sms, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace pop

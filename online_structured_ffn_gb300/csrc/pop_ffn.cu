@@ -46,6 +46,7 @@ struct pop_ffn {
   int* step = nullptr;
   unsigned* err = nullptr;
   unsigned* fsync = nullptr;  // inter-CTA counters of the decode kernels
+  unsigned epoch = 0;  // B > 1 decode calls so far: the selection flag of call e reads e
   bool partitioned = false;
   bool selected = false;
   uint64_t wait_ns = 2000000000ull;
@@ -156,21 +157,21 @@ cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
   return cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
 }
 
-// gate/up over positions [0, nRC) of rc for B tokens: z, zk (positions >= nC) and scores (< nC).
-pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nRC, int nC, cudaStream_t st) {
-  DecodeTcArgs a{};
+// gate/up over the positions of rc = [C (nC) | R (nR)] for B tokens: z of the candidates (zc),
+// their scores, and the z planes of R.
+pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st) {
+  GateUpTcArgs a{};
   a.Wp = h->Wp;
   a.D = h->D;
+  a.N = h->N;
   a.B = B;
   a.NP = round_up(B, 16);
-  a.rows = nRC;
-  a.K = h->D;
-  a.N = h->N;
   a.rc = rc;
   a.nC = nC;
+  a.nR = nR;
   a.n2 = h->n2;
-  a.z = h->z;
-  a.ldz = nRC;
+  a.zc = h->z;
+  a.ldzc = round_up(B, 4);
   a.zk = h->zk;
   a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
   a.ldk = h->ldk;
@@ -184,35 +185,46 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nR
   return POP_OK;
 }
 
-// y[b] = sum over the kept items j of z[b][j] W2[:, channel of j] for B tokens: the nR items with
-// channels ch_r[], then the k items with channels ch_s[].
-pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, const int* ch_s, int k, void* y, cudaStream_t st) {
-  const int nK = nR + k;
-  if (nK <= 0) {
+// The selection of this decode step (decode: when there are candidates) and y[b] = sum over the
+// kept items of z[b][item] W2[:, channel]: the nR items with channels ch_r[], then the k selected
+// candidates. decode = false: the dense path (no selection, no step count).
+pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decode, void* y, cudaStream_t st) {
+  if (nR + k <= 0) {
     const size_t bytes = static_cast<size_t>(B) * h->D * (h->cfg.out_f32 ? 4 : 2);
     POP_CUDA(h, cudaMemsetAsync(y, 0, bytes, st));
-    return POP_OK;
   }
-  DecodeTcArgs a{};
+  DownTcArgs a{};
   a.Wp = h->Wp;
   a.D = h->D;
+  a.N = h->N;
   a.B = B;
   a.NP = round_up(B, 16);
-  a.rows = h->D;
-  a.K = nK;
-  a.N = h->N;
+  a.nR = nR;
+  a.kbr = (nR + 63) / 64;
+  a.k = k;
   a.ch_r = ch_r;
-  a.ch_s = ch_s;
-  a.nR_items = nR;
+  a.ch_s = h->ch_s;
+  a.zk = h->zk;
+  a.zk_lo_off = static_cast<size_t>(h->cfg.max_batch) * h->ldk;
+  a.ldk = h->ldk;
   a.y = y;
   a.out_f32 = h->cfg.out_f32;
+  a.sel = decode && h->cnt.n_C > 0 ? 1 : 0;
+  a.scores = h->scores;
+  a.zc = h->z;
+  a.ldzc = round_up(B, 4);
+  a.rc = h->rc;
+  a.nC = h->cnt.n_C;
+  a.period = h->cfg.period;
+  a.memory = h->memory;
+  a.S = h->S;
+  a.step = h->step;
+  a.count_step = decode ? 1 : 0;
+  a.flag = h->fsync + 5;
+  a.epoch = decode ? ++h->epoch : 0;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
-  CUtensorMap zm, zlm;
-  if (!encode_tokens_map(&zm, h->zk, nK, B, h->ldk, a.NP) ||
-      !encode_tokens_map(&zlm, h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, nK, B, h->ldk, a.NP))
-    return fail(h, POP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed for z");
-  POP_CUDA(h, launch_down_tc(zm, zlm, a, h->num_sms, st));
+  POP_CUDA(h, launch_down_tc(a, h->num_sms, st));
   return POP_OK;
 }
 
@@ -303,7 +315,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   h->ldZ = round_up(N, 128);
   h->ldPart = h->ldZ;
   h->ypart_parts = 2 * h->num_sms;
-  h->ldk = round_up(N, 8);
+  h->ldk = round_up(N + 128, 8);  // the selected items start at a 64-aligned column after R
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   auto bail = [&](cudaError_t err, const char* where) {
@@ -325,7 +337,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->rc, N);
   POP_ALLOC(h->P, N);
   POP_ALLOC(h->idx_all, N);
-  POP_ALLOC(h->z, static_cast<size_t>(cfg->max_batch) * N);
+  POP_ALLOC(h->z, static_cast<size_t>(round_up(cfg->max_batch, 4)) * N);
   POP_ALLOC(h->scores, N);
   POP_ALLOC(h->memory, N);
   POP_ALLOC(h->S, N);
@@ -342,6 +354,10 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   if (h->ch_s && (e = cudaMemsetAsync(h->ch_s, 0, sizeof(int) * N, st)) != cudaSuccess)
+    return bail(e, "cudaMemsetAsync");
+  // the z planes' columns between R and the selected items are read (against zero weights): keep
+  // them finite
+  if (h->zk && (e = cudaMemsetAsync(h->zk, 0, 2 * sizeof(uint16_t) * cfg->max_batch * h->ldk, st)) != cudaSuccess)
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection
@@ -471,7 +487,7 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: x, y must be 16-byte aligned");
   if (!h->partitioned) return fail(h, POP_ERR_STATE, "pop_decode_step: no partition (run a prefill first)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int nC = h->cnt.n_C, nR = h->cnt.n_R, nRC = nC + nR;
+  const int nC = h->cnt.n_C, nR = h->cnt.n_R;
   prof_begin(h);
   if (B == 1) {
     const int grid = h->num_sms * 4;
@@ -489,17 +505,13 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     prof_mark(h, 3, st);
     prof_mark(h, 4, st);
   } else {
+    // gate/up, then the down GEMM over R and the selected items with the selection inside
     prof_mark(h, 0, st);
-    if (nRC > 0) {
-      pop_status s = gateup_tc(h, static_cast<const uint16_t*>(x), B, h->rc, nRC, nC, st);
-      if (s != POP_OK) return s;
-    }
+    pop_status s = gateup_tc(h, static_cast<const uint16_t*>(x), B, h->rc, nC, nR, st);
+    if (s != POP_OK) return s;
     prof_mark(h, 1, st);
-    POP_CUDA(h, launch_select_bn(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
-    POP_CUDA(h, launch_pack_selected(h->S, h->cnt.k, nC, h->rc, h->N, h->ch_s, h->z, nRC, B, h->zk,
-                                     h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk, h->ldk, nR, h->err, st));
     prof_mark(h, 2, st);
-    pop_status s = down_tc(h, B, h->rc + nC, nR, h->ch_s, h->cnt.k, y, st);
+    s = down_tc(h, B, h->rc + nC, nR, h->cnt.k, true, y, st);
     if (s != POP_OK) return s;
     prof_mark(h, 3, st);
     prof_mark(h, 4, st);
@@ -523,9 +535,9 @@ pop_status pop_ffn_dense_ref(pop_ffn_t h, const void* X, int M, void* Y, void* s
     return POP_OK;
   }
   // 2 <= M <= max_batch: the decode kernels over every channel (all positions count as retained)
-  pop_status s = gateup_tc(h, static_cast<const uint16_t*>(X), M, h->idx_all, h->N, 0, st);
+  pop_status s = gateup_tc(h, static_cast<const uint16_t*>(X), M, h->idx_all, 0, h->N, st);
   if (s != POP_OK) return s;
-  return down_tc(h, M, h->idx_all, h->N, h->ch_s, 0, Y, st);
+  return down_tc(h, M, h->idx_all, h->N, 0, false, Y, st);
 }
 
 pop_status pop_get_partition(pop_ffn_t h, int* R, int* C, int* P) {

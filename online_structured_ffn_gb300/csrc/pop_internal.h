@@ -26,39 +26,64 @@ enum : unsigned {
 cudaError_t launch_pack(const uint16_t* Wg, const uint16_t* W1, const uint16_t* W2, uint16_t* Wp, float* n2,
                         int D, int N, cudaStream_t st);
 
-// ---- decode step for B > 1 (pop_decode_tc.cu): stream-K skinny GEMMs on tcgen05
+// ---- decode step for B > 1 (pop_decode_tc.cu): two skinny GEMMs on tcgen05
 // The B operand of a decode GEMM: `rows` token rows of `inner` bf16, `ld` elements apart, box
 // {64, NP} (rows NP > `rows` read as zero).
 bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int NP);
-struct DecodeTcArgs {
+struct GateUpTcArgs {
   const uint16_t* Wp;    // packed weights
-  int D;
+  int D, N;
   int B, NP;             // tokens, and tokens padded to a multiple of 16 (the MMA's N)
-  int rows;              // M extent: positions |R u C| (gate/up) or D (down)
-  int K;                 // reduction extent: D (gate/up) or the kept items |R| + k (down)
-  int N;                 // channel count, for the index guards
-  const int* rc;         // gate/up: position -> channel ([C | R])
-  const int* ch_r;       // down: channels of the items j < nR_items (R)
-  const int* ch_s;       // down: channels of the items j >= nR_items (the selected candidates)
-  int nR_items;
-  int nC;                // gate/up: positions below nC are candidates
+  const int* rc;         // position -> channel: [C | R]
+  int nC, nR;
   const float* n2;       // ||W2[:, c]||
-  float* z;              // gate/up out: fp32 [B][ldz]
-  int ldz;
-  uint16_t* zk;          // gate/up out: z of R positions at [b][p - nC], bf16 hi part
-  uint16_t* zk_lo;       // ... and bf16 lo part z - hi
+  float* zc;             // out: z of the candidate positions, fp32 [nC][ldzc] (tokens contiguous)
+  int ldzc;              // round_up(B, 4)
+  uint16_t* zk;          // out: z of R as bf16 hi parts at [b][p - nC] (row stride ldk)
+  uint16_t* zk_lo;       // ... and bf16 lo parts z - hi
   int ldk;
-  float* scores;         // gate/up out: [nC]
-  void* y;               // down out: [B][D], fp32 or bf16
-  int out_f32;
-  int split;             // CTAs per tile along K (a cluster); set by the launcher
+  float* scores;         // out: [nC]
+  // work split (set by the launcher)
+  int units, rows_cap, ks, stages;
   unsigned* err;
   uint64_t wait_ns;
 };
-cudaError_t launch_gateup_tc(const CUtensorMap& x_map, const DecodeTcArgs& args, int num_sms, cudaStream_t st);
-// zk_map / zk_lo_map: the hi and lo bf16 planes of z over the kept items
-cudaError_t launch_down_tc(const CUtensorMap& zk_map, const CUtensorMap& zk_lo_map, const DecodeTcArgs& args,
-                           int num_sms, cudaStream_t st);
+struct DownTcArgs {
+  const uint16_t* Wp;
+  int D, N;
+  int B, NP;
+  int nR;                // R items: k-blocks [0, kbr) of the z planes' columns [0, nR)
+  int kbr;               // ceil(nR / 64); the selected items start at column 64 * kbr
+  int k;                 // selected candidates
+  const int* ch_r;       // channels of R (ascending)
+  int* ch_s;             // channels of the selected candidates (written by the selecting CTA)
+  const uint16_t* zk;    // z planes: hi [b][ldk], lo at zk + zk_lo_off
+  size_t zk_lo_off;
+  int ldk;
+  void* y;               // out: [B][D], fp32 or bf16
+  int out_f32;
+  // selection by the first cluster (sel = 1, decode with candidates)
+  int sel;
+  const float* scores;   // [nC] this step's candidate scores
+  const float* zc;       // [nC][ldzc] candidates' z
+  int ldzc;
+  const int* rc;         // position -> channel, C first
+  int nC, period;
+  float* memory;
+  int* S;
+  int* step;
+  int count_step;        // 1: advance the step counter (decode)
+  unsigned* flag;        // selection of step `epoch` complete when *flag == epoch
+  unsigned epoch;
+  // work split (set by the launcher)
+  int split, units;
+  unsigned* err;
+  uint64_t wait_ns;
+};
+// gate/up over R u C: z of the candidates, their scores, and the z planes of R
+cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int num_sms, cudaStream_t st);
+// the selection (when args.sel), then y = sum over R and the selected items of z W2[:, channel]
+cudaError_t launch_down_tc(DownTcArgs args, int num_sms, cudaStream_t st);
 
 // ---- decode step for B = 1 (pop_decode1.cu): gate/up with in-kernel top-k, tiled down
 struct DecodeB1Args {
@@ -101,15 +126,6 @@ cudaError_t launch_partition(const float* sumsq, const float* n2, float* I, int 
 // Candidate selection for one decode step (periodic memory, top-k, step counter).
 cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
                           unsigned* err, cudaStream_t st);
-// The same for B > 1 (the top-k only), launched with programmatic dependent launch.
-cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
-                             unsigned* err, cudaStream_t st);
-// The selected candidates' side of the B > 1 down projection: ch_s[j] = rc[S[j]] and the hi / lo
-// bf16 parts of z[b][S[j]] at zk[b][nR + j] / zk_lo[b][nR + j], for j < k, b < B. Many CTAs,
-// launched with programmatic dependent launch.
-cudaError_t launch_pack_selected(const int* S, int k, int nC, const int* rc, int N, int* ch_s, const float* z,
-                                 int ldz, int B, uint16_t* zk, uint16_t* zk_lo, int ldk, int nR, unsigned* err,
-                                 cudaStream_t st);
 // sumsq[i] (+)= sum over rows p < rows of part[p * ld + i], p ascending.
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
                               cudaStream_t st);

@@ -93,55 +93,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   if (threadIdx.x == 0) *step = t + 1;
 }
 
-// ------------------------------------------------------------------ selection for B > 1
-// The top-k of k_select, launched with programmatic dependent launch: nothing of this step is read
-// before griddepcontrol.wait.
-__global__ void __launch_bounds__(SEL_THREADS, 1)
-    k_select_bn(const float* __restrict__ scores, float* __restrict__ memory, int nC, int k, int period,
-                int* __restrict__ step, int* __restrict__ S, unsigned* __restrict__ err) {
-  extern __shared__ uint32_t keys[];
-  __shared__ RadixScratch<SEL_THREADS> sc;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int t = *step;
-  bool ok = true;
-  if (nC > 0)
-    ok = select_step<SEL_THREADS>(
-        threadIdx.x, [&](int i) { return scores[i]; }, memory, nC, k, period, (t % period) == 0, keys, S, sc,
-        BlockSync());
-  if (!ok && threadIdx.x == 0) atomicOr(err, DEVERR_TOPK);
-  __syncthreads();
-  if (threadIdx.x == 0) *step = t + 1;
-}
-
-// The selected candidates' side of the down projection, one thread per (token b, selected item j),
-// j fastest so that S and the z planes are read / written in runs along j.
-__global__ void __launch_bounds__(256)
-    k_pack_selected(const int* __restrict__ S, int k, int nC, const int* __restrict__ rc, int N,
-                    int* __restrict__ ch_s, const float* __restrict__ z, int ldz, int B, uint16_t* __restrict__ zk,
-                    uint16_t* __restrict__ zk_lo, int ldk, int nR, unsigned* __restrict__ err) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= static_cast<long long>(k) * B) return;
-  const int b = static_cast<int>(e / k), j = static_cast<int>(e - static_cast<long long>(b) * k);
-  int pos = S[j];
-  if (static_cast<unsigned>(pos) >= static_cast<unsigned>(nC)) {
-    atomicOr(err, DEVERR_INDEX);
-    pos = 0;
-  }
-  if (b == 0) {
-    const int c = rc[pos];
-    if (static_cast<unsigned>(c) >= static_cast<unsigned>(N)) atomicOr(err, DEVERR_INDEX);
-    ch_s[j] = static_cast<unsigned>(c) < static_cast<unsigned>(N) ? c : 0;
-  }
-  const float zz = z[static_cast<size_t>(b) * ldz + pos];
-  const __nv_bfloat16 hi = __float2bfloat16_rn(zz);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(zz - __bfloat162float(hi));
-  zk[static_cast<size_t>(b) * ldk + nR + j] = *reinterpret_cast<const uint16_t*>(&hi);
-  zk_lo[static_cast<size_t>(b) * ldk + nR + j] = *reinterpret_cast<const uint16_t*>(&lo);
-}
-
 // ------------------------------------------------------------------ channel sums of squares
 __global__ void k_fold_sumsq(const float* __restrict__ part, int rows, int ld, int N, float* __restrict__ sumsq,
                              int accumulate) {
@@ -171,42 +122,6 @@ cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int
   }
   k_select<<<1, SEL_THREADS, smem, st>>>(scores, memory, nC, k, period, step, S, err);
   return cudaGetLastError();
-}
-
-template <class K, class... Args>
-static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-cudaError_t launch_select_bn(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
-                             unsigned* err, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(nC > 0 ? nC : 1) * sizeof(uint32_t);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_select_bn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  return launch_pdl(k_select_bn, dim3(1), dim3(SEL_THREADS), smem, st, scores, memory, nC, k, period, step, S, err);
-}
-
-cudaError_t launch_pack_selected(const int* S, int k, int nC, const int* rc, int N, int* ch_s, const float* z,
-                                 int ldz, int B, uint16_t* zk, uint16_t* zk_lo, int ldk, int nR, unsigned* err,
-                                 cudaStream_t st) {
-  const long long n = static_cast<long long>(k) * B;
-  if (n <= 0) return cudaSuccess;
-  return launch_pdl(k_pack_selected, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, S, k, nC, rc,
-                    N, ch_s, z, ldz, B, zk, zk_lo, ldk, nR, err);
 }
 
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
