@@ -88,6 +88,7 @@ struct DnCfg {
 struct TcCtl {
   uint64_t full[TC_MAX_STAGES];
   uint64_t empty[TC_MAX_STAGES];
+  uint64_t afull[TC_MAX_STAGES];  // down: the stage's slab tile (bulk copy) has landed
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -214,11 +215,12 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
     if (!update)  // the held selection of the last update step
       for (int i = tid; i < (k + 3) / 4; i += TC_THREADS)
         cp_async16(sb + static_cast<uint32_t>(o_S) + 16u * i, a.S + 4 * i, 4u * min(4, k - 4 * i));
-    if (zin) {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (zin) {  // z lands while the top-k runs
       const int nz = nC * (a.ldzc / 4);  // ldzc is a multiple of 4: whole 16-byte chunks
       for (int i = tid; i < nz; i += TC_THREADS) cp_async16(sb + static_cast<uint32_t>(o_z) + 16u * i, a.zc + 4 * i, 16u);
     }
-    cp_async_wait_all();
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 1;" ::: "memory");
   }
   __syncthreads();
   __shared__ int s_sel;
@@ -230,6 +232,7 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
           sS, rsc, ProdSync());
     if (tid == 0) s_sel = sel ? 1 : 0;
   }
+  if (small) cp_async_wait_all();  // z of the candidates
   __syncthreads();
   if (update && small)
     for (int j = tid; j < k; j += TC_THREADS) a.S[j] = sS[j];
@@ -578,6 +581,394 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ decode slabs (built per partition)
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// One 16-byte chunk per thread (grid-stride): chunk e of the gate/up slab is position pos = e % 8 of
+// A row ar of k-block kb of tile t; it holds data chunk c = pos ^ (ar % 8) (the 128-byte swizzle).
+__global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __restrict__ rc, int D, int N,
+                                GuSlabGeom g, uint16_t* __restrict__ slab, unsigned* __restrict__ err) {
+  const size_t total = static_cast<size_t>(g.T) * g.KB * g.arows * 8;
+  const int grows = (g.RT + 7) / 8 * 8;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(e & 7);
+    size_t rest = e >> 3;
+    const int ar = static_cast<int>(rest % g.arows);
+    rest /= g.arows;
+    const int kb = static_cast<int>(rest % g.KB);
+    const int t = static_cast<int>(rest / g.KB);
+    const int c = pos ^ (ar & 7);
+    int j, gu;
+    if (g.paired) {
+      const int rem = ar & 31;
+      gu = rem >> 4;
+      j = 16 * (ar >> 5) + (rem & 15);
+    } else {
+      gu = ar >= grows ? 1 : 0;
+      j = gu ? ar - grows : ar;
+    }
+    const int p = t * g.RT + j;
+    const int d = kb * TC_BK + 8 * c;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < g.RT && p < g.P && d < D) {
+      int ch = rc[p];
+      if (static_cast<unsigned>(ch) >= static_cast<unsigned>(N)) {
+        atomicOr(err, DEVERR_INDEX);
+        ch = 0;
+      }
+      v = *reinterpret_cast<const uint4*>(Wp + static_cast<size_t>(ch) * 3 * D + static_cast<size_t>(gu) * D + d);
+    }
+    *reinterpret_cast<uint4*>(slab + e * 8) = v;
+  }
+}
+
+// Chunk e of the down slab: position pos = e % 8 of item i of output half h of item block b of
+// output slice o; it holds the 8 outputs 128 o + 64 h + 8 c, c = pos ^ (i % 8), of R item 64 b + i.
+__global__ void k_build_dn_slab(const uint16_t* __restrict__ Wp, const int* __restrict__ rc, int nC, int nR, int D,
+                                int N, int kbr, uint16_t* __restrict__ slab, unsigned* __restrict__ err) {
+  const int O = (D + TC_BM - 1) / TC_BM;
+  const size_t total = static_cast<size_t>(O) * kbr * 2 * TC_BK * 8;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(e & 7);
+    size_t rest = e >> 3;
+    const int i = static_cast<int>(rest & 63);
+    rest >>= 6;
+    const int h = static_cast<int>(rest & 1);
+    rest >>= 1;
+    const int b = static_cast<int>(rest % kbr);
+    const int o = static_cast<int>(rest / kbr);
+    const int c = pos ^ (i & 7);
+    const int item = b * TC_BK + i;
+    const int d = o * TC_BM + 64 * h + 8 * c;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (item < nR && d < D) {
+      int ch = rc[nC + item];
+      if (static_cast<unsigned>(ch) >= static_cast<unsigned>(N)) {
+        atomicOr(err, DEVERR_INDEX);
+        ch = 0;
+      }
+      v = *reinterpret_cast<const uint4*>(Wp + static_cast<size_t>(ch) * 3 * D + 2 * static_cast<size_t>(D) + d);
+    }
+    *reinterpret_cast<uint4*>(slab + e * 8) = v;
+  }
+}
+
+// ------------------------------------------------------------------ gate/up over R u C from the slab
+// One CTA per SM; CTA w streams tiles w, w + grid, ... Warp 0 lane 0 issues, per stage of KS
+// k-blocks, one bulk copy of the tile's KS contiguous A images and KS TMA boxes of x; warp 1 lane 0
+// issues the MMAs (one per K = 16 when gate and up share the tile's rows, two otherwise) and owns
+// TMEM; warps 2-5 are the epilogue (TMEM lane quarter = warp % 4). The slab is constant between
+// partitions, so the first GU_PRE stages' copies go out before griddepcontrol.wait; their x boxes
+// after it.
+constexpr int GS_THREADS = 192;
+template <int NP, bool PAIRED>
+__global__ void __launch_bounds__(GS_THREADS, 1)
+    k_gateup_slab(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ GateUpSlabArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ TcCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const GuSlabGeom g = a.geom;
+  const int W = static_cast<int>(gridDim.x), w = static_cast<int>(blockIdx.x);
+  const int KS = a.ks, STAGES = a.stages;
+  const uint32_t ABYTES = static_cast<uint32_t>(g.arows) * 128u;
+  const uint32_t XBYTES = NP * 128u;
+  const uint32_t STAGE = KS * (ABYTES + XBYTES);
+  const int KBS = (g.KB + KS - 1) / KS;  // stages per tile
+  const uint32_t UP_OFF = static_cast<uint32_t>((g.RT + 7) / 8 * 8) * 128u;  // up rows (unpaired tiles)
+  // Each CTA walks the k-blocks from its own starting stage: all CTAs read the same x tiles, and
+  // moving in step they would all ask L2 for the same lines at once.
+  const uint32_t rot = static_cast<uint32_t>(w) * 5u;
+  volatile int* abort_flag = &ctl.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl.tfull[b], 1);
+      mbar_init(&ctl.tempty[b], 4);
+    }
+    mbar_init(&ctl.drain, 1);
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&mapX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, TC_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  pdl_trigger();
+
+  auto fail = [&]() {
+    if (!*abort_flag) {
+      *abort_flag = 1;
+      atomicOr(a.err, DEVERR_TIMEOUT_DECODE_TC);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer (one thread)
+      uint32_t issued = 0, x_done = 0;
+      bool ok = true, waited = false;
+      auto stage_kb = [&](uint32_t i, int& kb0, int& nk) {
+        kb0 = static_cast<int>((i + rot) % static_cast<uint32_t>(KBS)) * KS;
+        nk = min(KS, g.KB - kb0);
+      };
+      auto issue_x = [&](uint32_t i) {
+        int kb0, nk;
+        stage_kb(i, kb0, nk);
+        uint8_t* sx = smem + (i % static_cast<uint32_t>(STAGES)) * STAGE + KS * ABYTES;
+        for (int u = 0; u < nk; ++u)
+          tma_load_2d(sx + u * XBYTES, &mapX, &ctl.full[i % STAGES], (kb0 + u) * TC_BK, 0);
+      };
+      for (int t = w; t < g.T && ok; t += W) {
+        for (int sbk = 0; sbk < KBS; ++sbk) {
+          const int s = static_cast<int>(issued % static_cast<uint32_t>(STAGES));
+          const uint32_t ph = (issued / static_cast<uint32_t>(STAGES)) & 1u;
+          if (!mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, a.wait_ns, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          int kb0, nk;
+          stage_kb(issued, kb0, nk);
+          mbar_arrive_expect_tx(&ctl.full[s], static_cast<uint32_t>(nk) * (ABYTES + XBYTES));
+          bulk_g2s(smem + s * STAGE, a.slab + (static_cast<size_t>(t) * g.KB + kb0) * g.arows * 64,
+                   static_cast<uint32_t>(nk) * ABYTES, &ctl.full[s]);
+          if (waited) {
+            issue_x(issued);
+            x_done = issued + 1;
+          } else if (issued + 1 >= static_cast<uint32_t>(STAGES < GU_PRE ? STAGES : GU_PRE)) {
+            pdl_wait();  // x of this step is complete once the previous kernel is
+            waited = true;
+            for (uint32_t i = x_done; i <= issued; ++i) issue_x(i);
+            x_done = issued + 1;
+          }
+          ++issued;
+        }
+      }
+      // x boxes still owed (fewer stages than GU_PRE, or an abort before the wait): issued in any case,
+      // so that every issued stage's barrier completes once its bytes have landed
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+        for (uint32_t i = x_done; i < issued; ++i) issue_x(i);
+        x_done = issued;
+      }
+      // no copy of this CTA may be in flight when it exits
+      const uint32_t lo = x_done > static_cast<uint32_t>(STAGES) ? x_done - STAGES : 0;
+      for (uint32_t i = lo; i < x_done; ++i) {
+        volatile int never = 0;
+        if (!mbar_wait_bounded(&ctl.full[i % STAGES], (i / STAGES) & 1u, TC_DRAIN_NS, &never)) fail();
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (one thread)
+      const uint32_t idesc = idesc_bf16_f32(TC_BM, NP, false, false);
+      uint32_t consumed = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = w; t < g.T && ok; t += W, ++it) {
+        const int buf = it & 1;
+        if (!mbar_wait_bounded(&ctl.tempty[buf], ((it >> 1) & 1) ^ 1, a.wait_ns, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * TC_HALF;
+        for (int sbk = 0; sbk < KBS; ++sbk) {
+          const int s = static_cast<int>(consumed % static_cast<uint32_t>(STAGES));
+          const uint32_t ph = (consumed / static_cast<uint32_t>(STAGES)) & 1u;
+          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nk = min(KS, g.KB - static_cast<int>((static_cast<uint32_t>(sbk) + rot) % KBS) * KS);
+          const uint32_t sa = smem_u32(smem + s * STAGE);
+          // descriptors once per stage; a K step of 16 moves the start address by 32 bytes (+2)
+          uint64_t ad = smem_desc_sw128(sa, 16u, 1024u);
+          uint64_t bd = smem_desc_sw128(sa + KS * ABYTES, 16u, 1024u);
+          const uint64_t up = UP_OFF >> 4;
+          for (int u = 0; u < nk; ++u) {
+            const uint32_t first = (sbk == 0 && u == 0) ? 0u : 1u;
+            if (PAIRED) {
+              umma_f16(d_tmem, ad, bd, idesc, first);
+              umma_f16(d_tmem, ad + 2, bd + 2, idesc, 1u);
+              umma_f16(d_tmem, ad + 4, bd + 4, idesc, 1u);
+              umma_f16(d_tmem, ad + 6, bd + 6, idesc, 1u);
+            } else {
+              const uint32_t du = d_tmem + static_cast<uint32_t>(NP);
+              umma_f16(d_tmem, ad, bd, idesc, first);
+              umma_f16(du, ad + up, bd, idesc, first);
+              umma_f16(d_tmem, ad + 2, bd + 2, idesc, 1u);
+              umma_f16(du, ad + up + 2, bd + 2, idesc, 1u);
+              umma_f16(d_tmem, ad + 4, bd + 4, idesc, 1u);
+              umma_f16(du, ad + up + 4, bd + 4, idesc, 1u);
+              umma_f16(d_tmem, ad + 6, bd + 6, idesc, 1u);
+              umma_f16(du, ad + up + 6, bd + 6, idesc, 1u);
+            }
+            ad += ABYTES >> 4;
+            bd += XBYTES >> 4;
+          }
+          umma_commit(&ctl.empty[s]);
+          ++consumed;
+        }
+        if (!ok) break;
+        umma_commit(&ctl.tfull[buf]);
+      }
+      umma_commit(&ctl.drain);
+      volatile int never = 0;
+      if (!mbar_wait_bounded(&ctl.drain, 0, TC_DRAIN_NS, &never)) fail();
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    pdl_wait();  // z, scores and the z planes may still be read by the previous step's kernels
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127
+    constexpr int NH = NP / 2;
+    int it = 0;
+    for (int t = w; t < g.T; t += W, ++it) {
+      const int buf = it & 1;
+      // paired: lane l < 16 holds gate, l + 16 up, of position 16 q + l % 16 (tokens split in two
+      // halves between them); unpaired: lane l holds gate (columns [0, NP)) and up ([NP, 2 NP)) of
+      // position 32 q + l
+      const int j = PAIRED ? 16 * q + (lane & 15) : 32 * q + lane;
+      const int p = t * g.RT + j;
+      const bool valid = j < g.RT && p < g.P;
+      const bool cand = valid && p < a.nC;
+      const int half = PAIRED ? (lane >> 4) : 0;
+      float n2v = 0.f;
+      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldg(a.rc + p), a.N, a.err));
+      if (et == 0)
+        ctl.seg_ok[buf] = mbar_wait_bounded(&ctl.tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
+      epi_bar();
+      if (!ctl.seg_ok[buf]) {
+        if (et == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf) * TC_HALF;
+      if (PAIRED) {
+        float acc[NP];
+#pragma unroll
+        for (int c = 0; c < NP; c += 16) {
+          uint32_t t16[16];
+          tmem_ld16(taddr + c, t16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(t16[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
+        const int b0 = half * NH;
+        float zz[NH];
+#pragma unroll
+        for (int i = 0; i < NH; ++i) {
+          const float mine = half ? acc[i] : acc[NH + i];
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+          const float gg = half ? other : acc[i];
+          const float uu = half ? acc[NH + i] : other;
+          zz[i] = silu_t(gg) * uu;
+        }
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < NH; ++i)
+          if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (cand) {
+          float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc + b0);
+#pragma unroll
+          for (int i4 = 0; i4 < NH / 4; ++i4)
+            if (b0 + 4 * i4 < a.ldzc) dst[i4] = make_float4(zz[4 * i4], zz[4 * i4 + 1], zz[4 * i4 + 2], zz[4 * i4 + 3]);
+          if (half == 0) a.scores[p] = m * n2v;
+        } else if (valid) {
+#pragma unroll
+          for (int i = 0; i < NH; ++i) {
+            if (b0 + i < a.B) {
+              uint16_t h16, l16;
+              split_bf16(zz[i], h16, l16);
+              const size_t o = static_cast<size_t>(b0 + i) * a.ldk + (p - a.nC);
+              a.zk[o] = h16;
+              a.zk_lo[o] = l16;
+            }
+          }
+        }
+      } else {
+        float gv[NP], uv[NP];
+#pragma unroll
+        for (int c = 0; c < NP; c += 16) {
+          uint32_t t16[16];
+          tmem_ld16(taddr + c, t16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) gv[c + i] = __uint_as_float(t16[i]);
+          tmem_ld16(taddr + NP + c, t16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) uv[c + i] = __uint_as_float(t16[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
+        if (valid) {
+          float zz[NP];
+          float m = 0.f;
+#pragma unroll
+          for (int b = 0; b < NP; ++b) {
+            zz[b] = silu_t(gv[b]) * uv[b];
+            if (b < a.B) m = fmaxf(m, fabsf(zz[b]));
+          }
+          if (cand) {
+            float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc);
+#pragma unroll
+            for (int b4 = 0; b4 < NP / 4; ++b4)
+              if (4 * b4 < a.ldzc) dst[b4] = make_float4(zz[4 * b4], zz[4 * b4 + 1], zz[4 * b4 + 2], zz[4 * b4 + 3]);
+            a.scores[p] = m * n2v;
+          } else {
+#pragma unroll
+            for (int b = 0; b < NP; ++b) {
+              if (b < a.B) {
+                uint16_t h16, l16;
+                split_bf16(zz[b], h16, l16);
+                const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
+                a.zk[o] = h16;
+                a.zk_lo[o] = l16;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TC_TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ selection + down over R u S
 template <int NP>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant__ DownTcArgs a) {
@@ -609,7 +1000,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   const int unit0 = ci - a.sel, nunits = static_cast<int>(gridDim.x) / SK - a.sel;
   const int U = a.units;
   const int G = a.D / 8;  // output groups of 8 (16 bytes); a unit is a range of whole groups
-  auto unit_lo = [&](int u) { return 8 * static_cast<int>(static_cast<long long>(u) * G / U); };
+  const bool slab = a.dslab != nullptr;  // R tiles from the slab; units are its 128-output slices
+  auto unit_lo = [&](int u) {
+    return slab ? min(a.D, TC_BM * u) : 8 * static_cast<int>(static_cast<long long>(u) * G / U);
+  };
   // this CTA's k-blocks: R blocks [r0, r1), then selected blocks [s0, s1) (block kbr + t holds
   // selected items 64 t ..)
   const int kbs = (a.k + TC_BK - 1) / TC_BK;
@@ -621,6 +1015,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctl.full[s], TC_PROD_THREADS);
       mbar_init(&ctl.empty[s], 1);
+      mbar_init(&ctl.afull[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.tfull[b], 1);
@@ -768,7 +1163,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
             break;
           }
         }
-        if (bi < wlo || bi >= whi) fill(bi);
+        const bool from_slab = slab && bi < nrs;
+        // R blocks from the slab go in an order rotated per unit (the units of a rank read the same z
+        // columns; in step they would ask L2 for the same lines at once)
+        const int rb = from_slab ? (bi + 7 * unit) % nrs : bi;
+        if (!from_slab && (bi < wlo || bi >= whi)) fill(bi);
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1u;
         bool got = true;
@@ -782,18 +1181,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
           break;
         }
         const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        issue_a(bi, sa, d0, dok);
+        if (from_slab) {
+          if (warp == 0 && lane == 0) {
+            mbar_arrive_expect_tx(&ctl.afull[s], Cfg::A_BYTES);
+            bulk_g2s(smem + s * STAGE_BYTES, a.dslab + (static_cast<size_t>(unit) * a.kbr + r0 + rb) * (Cfg::A_BYTES / 2),
+                     Cfg::A_BYTES, &ctl.afull[s]);
+          }
+        } else {
+          if (warp == 0 && lane == 0) mbar_arrive(&ctl.afull[s]);
+          issue_a(bi, sa, d0, dok);
+        }
         if (issued < static_cast<uint32_t>(pre)) {
           if (issued + 1 == static_cast<uint32_t>(pre)) {
             // the z planes of this step exist once the previous kernel has finished
             pdl_wait();
             for (int bj = 0; bj < pre; ++bj) {
-              issue_b(bj, smem_u32(smem + bj * STAGE_BYTES));
+              issue_b(slab ? (bj + 7 * unit) % nrs : bj, smem_u32(smem + bj * STAGE_BYTES));
               cp_async_arrive(&ctl.full[bj]);
             }
           }
         } else {
-          issue_b(bi, sa);
+          issue_b(rb, sa);
           cp_async_arrive(&ctl.full[s]);
         }
         ++issued;
@@ -803,8 +1211,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     // are only drained below through the copies of this warp
     if (issued < static_cast<uint32_t>(pre)) pdl_wait();
     if (!a.sel && a.count_step && blockIdx.x == 0 && threadIdx.x == 0) *a.step += 1;
-    // every copy this warp started must land before the CTA can exit
+    // every copy this warp started must land before the CTA can exit (the slab tiles: through their
+    // barriers, for the last STAGES stages issued; earlier ones were consumed by the MMAs)
     cp_async_wait_all();
+    if (warp == 0 && lane == 0) {
+      const uint32_t lo = issued > static_cast<uint32_t>(STAGES) ? issued - STAGES : 0;
+      for (uint32_t i = lo; i < issued; ++i) {
+        volatile int never = 0;
+        if (!mbar_wait_bounded(&ctl.afull[i % STAGES], (i / STAGES) & 1u, TC_DRAIN_NS, &never)) fail();
+      }
+    }
     __syncwarp();
   } else if (warp == TC_MMA_WARP) {
     if (lane == 0) {
@@ -824,7 +1240,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         for (int bi = 0; bi < nblk; ++bi) {
           const int s = consumed % STAGES;
           const uint32_t ph = (consumed / STAGES) & 1u;
-          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag)) {
+          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag) ||
+              !mbar_wait_bounded(&ctl.afull[s], ph, a.wait_ns, abort_flag)) {
             fail();
             ok = false;
             break;
@@ -832,13 +1249,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
           fence_proxy_async();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t sb = sa + Cfg::A_BYTES;
-#pragma unroll
-          for (int k = 0; k < TC_BK / 16; ++k) {
-            const uint32_t acc = (bi > 0 || k > 0) ? 1u : 0u;
-            umma_f16(d_tmem, smem_desc_sw128(sa + 2048u * k, TC_BK * 128, 1024u),
-                     smem_desc_sw128(sb + 32u * k, 16u, 1024u), idesc, acc);
-          }
+          // descriptors once per stage: a K step of 16 items moves A by 2048 bytes (+128), B by 32 (+2)
+          const uint64_t ad = smem_desc_sw128(sa, TC_BK * 128, 1024u);
+          const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, 16u, 1024u);
+          umma_f16(d_tmem, ad, bd, idesc, bi > 0 ? 1u : 0u);
+          umma_f16(d_tmem, ad + 128, bd + 2, idesc, 1u);
+          umma_f16(d_tmem, ad + 256, bd + 4, idesc, 1u);
+          umma_f16(d_tmem, ad + 384, bd + 6, idesc, 1u);
           umma_commit(&ctl.empty[s]);
           ++consumed;
         }
@@ -1083,7 +1500,7 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   // The split depends only on these sizes and the device: computed once per shape (the occupancy
   // queries cost host time on every step otherwise).
   struct Key {
-    int D, kbr, kbs, sel, sms, dev;
+    int D, kbr, kbs, sel, sms, dev, slab;
   };
   struct Entry {
     Key key;
@@ -1093,12 +1510,14 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   static int cache_n = 0;
   int dev = 0;
   (void)cudaGetDevice(&dev);
-  const Key key{a.D, a.kbr, kbs, sel, num_sms, dev};
+  const int slab = a.dslab != nullptr ? 1 : 0;
+  const Key key{a.D, a.kbr, kbs, sel, num_sms, dev, slab};
   int best_sk = 1, best_u = tiles;
   bool hit = false;
   for (int i = 0; i < cache_n; ++i) {
     const Key& c = cache[i].key;
-    if (c.D == key.D && c.kbr == key.kbr && c.kbs == key.kbs && c.sel == key.sel && c.sms == key.sms && c.dev == key.dev) {
+    if (c.D == key.D && c.kbr == key.kbr && c.kbs == key.kbs && c.sel == key.sel && c.sms == key.sms &&
+        c.dev == key.dev && c.slab == key.slab) {
       best_sk = cache[i].sk;
       best_u = cache[i].u;
       hit = true;
@@ -1129,7 +1548,7 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
     }
     if (ncl < 1) continue;
     int U = ncl < u64 ? ncl : u64;
-    if (U < tiles) U = tiles;
+    if (U < tiles || slab) U = tiles;  // with the slab, units are its 128-output slices
     const long long rows = 8LL * ((G + U - 1) / U);
     const long long rounds = (U + ncl - 1) / ncl;
     const long long blk = (a.kbr + sk - 1) / sk + (kbs + sk - 1) / sk;
@@ -1159,6 +1578,115 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, a);
 }
 }  // namespace
+
+GuSlabGeom gu_slab_geom(int P, int D, int num_sms) {
+  GuSlabGeom g{};
+  g.P = P;
+  g.KB = (D + TC_BK - 1) / TC_BK;
+  const int W = num_sms > 0 ? num_sms : 1;
+  // tiles of at most 128 positions, one per SM where the positions allow it
+  int T = P > 0 ? (P + 127) / 128 : 1;
+  if (T < W) T = P > 0 ? (W < (P + 15) / 16 ? W : (P + 15) / 16) : 1;
+  g.T = T > 0 ? T : 1;
+  g.RT = P > 0 ? (P + g.T - 1) / g.T : 1;
+  g.T = P > 0 ? (P + g.RT - 1) / g.RT : 1;
+  g.paired = g.RT <= GU_MAX_ROWS ? 1 : 0;
+  if (g.paired) {
+    const int jm = g.RT - 1;
+    g.arows = ((32 * (jm >> 4) + 16 + (jm & 15) + 1) + 7) / 8 * 8;
+  } else {
+    g.arows = 2 * ((g.RT + 7) / 8 * 8);
+  }
+  return g;
+}
+
+size_t gu_slab_elems(const GuSlabGeom& g) { return static_cast<size_t>(g.T) * g.KB * g.arows * 64; }
+
+size_t dn_slab_elems(int D, int nR) {
+  const size_t O = (D + TC_BM - 1) / TC_BM, kbr = (nR + TC_BK - 1) / TC_BK;
+  return O * kbr * TC_BK * TC_BM;
+}
+
+cudaError_t launch_build_slabs(const uint16_t* Wp, const int* rc, int nC, int nR, int D, int N, const GuSlabGeom& g,
+                               uint16_t* gu_slab, uint16_t* dn_slab, unsigned* err, cudaStream_t st) {
+  if (gu_slab && g.P > 0) {
+    k_build_gu_slab<<<1184, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (dn_slab && nR > 0) {
+    k_build_dn_slab<<<1184, 256, 0, st>>>(Wp, rc, nC, nR, D, N, (nR + TC_BK - 1) / TC_BK, dn_slab, err);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+namespace {
+// The slab gate/up stage: KS k-blocks (the most, up to 4, that leave three stages); past the ring,
+// room for the MMA's reads of 128 rows from the last A image's gate (and up) base.
+template <int NP>
+cudaError_t launch_gateup_slab_np(const CUtensorMap& xm, GateUpSlabArgs a, int num_sms, cudaStream_t st) {
+  const GuSlabGeom& g = a.geom;
+  if (g.P <= 0) return cudaSuccess;
+  const uint32_t ab = static_cast<uint32_t>(g.arows) * 128u, xb = NP * 128u;
+  const uint32_t up = g.paired ? 0u : static_cast<uint32_t>((g.RT + 7) / 8 * 8) * 128u;
+  const uint32_t budget = 227u * 1024u - 1024u - static_cast<uint32_t>(sizeof(TcCtl)) - 64u;
+  int ks = 1;
+  uint32_t slack = 0;
+  for (int k = 4; k >= 1; --k) {
+    const uint32_t stage = k * (ab + xb);
+    const uint32_t reach = (k - 1) * ab + up + TC_BM * 128u;  // end of the last MMA read from the stage base
+    const uint32_t sl = reach > stage ? reach - stage : 0u;
+    if (budget > sl && (budget - sl) / stage >= 3) {
+      ks = k;
+      slack = sl;
+      break;
+    }
+    if (k == 1) {
+      slack = sl;
+    }
+  }
+  const uint32_t stage = ks * (ab + xb);
+  int stages = static_cast<int>((budget - slack) / stage);
+  stages = stages > TC_MAX_STAGES ? TC_MAX_STAGES : stages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * stage + slack;
+  static size_t configured[2] = {0, 0};
+  const int pi = g.paired ? 1 : 0;
+  if (smem > configured[pi]) {
+    cudaError_t e = g.paired ? cudaFuncSetAttribute(k_gateup_slab<NP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(smem))
+                             : cudaFuncSetAttribute(k_gateup_slab<NP, false>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[pi] = smem;
+  }
+  a.ks = ks;
+  a.stages = stages;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(g.T < num_sms ? g.T : num_sms);
+  cfg.blockDim = dim3(GS_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return g.paired ? cudaLaunchKernelEx(&cfg, k_gateup_slab<NP, true>, xm, a)
+                  : cudaLaunchKernelEx(&cfg, k_gateup_slab<NP, false>, xm, a);
+}
+}  // namespace
+
+cudaError_t launch_gateup_slab(const CUtensorMap& x_map, GateUpSlabArgs args, int num_sms, cudaStream_t st) {
+  switch (args.NP) {
+    case 16: return launch_gateup_slab_np<16>(x_map, args, num_sms, st);
+    case 32: return launch_gateup_slab_np<32>(x_map, args, num_sms, st);
+    case 48: return launch_gateup_slab_np<48>(x_map, args, num_sms, st);
+    case 64: return launch_gateup_slab_np<64>(x_map, args, num_sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int num_sms, cudaStream_t st) {
   switch (args.NP) {

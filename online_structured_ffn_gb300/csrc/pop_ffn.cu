@@ -43,6 +43,10 @@ struct pop_ffn {
   uint16_t* zk = nullptr;  // [2][max_batch][ldk]: bf16 hi and lo parts of z of the kept items (R, then S)
   int ldk = 0;
   int* ch_s = nullptr;     // channels of the selected candidates, in S order
+  // B > 1 decode slabs (rebuilt at every partition): gate/up rows of R u C and down columns of R
+  GuSlabGeom gu_geom{};
+  uint16_t* gu_slab = nullptr;
+  uint16_t* dn_slab = nullptr;
   int* step = nullptr;
   unsigned* err = nullptr;
   unsigned* fsync = nullptr;  // inter-CTA counters of the decode kernels
@@ -120,7 +124,7 @@ void prof_end(pop_ffn* h) {
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
                   h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_s,
-                  h->step, h->err,     h->fsync};
+                  h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -157,8 +161,43 @@ cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
   return cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
 }
 
+// Rebuilds the B > 1 decode slabs from the current partition (stream-ordered after it).
+cudaError_t build_slabs(pop_ffn* h, cudaStream_t st) {
+  if (!h->gu_slab) return cudaSuccess;
+  return launch_build_slabs(h->Wp, h->rc, h->cnt.n_C, h->cnt.n_R, h->D, h->N, h->gu_geom, h->gu_slab, h->dn_slab,
+                            h->err, st);
+}
+
 // gate/up over the positions of rc = [C (nC) | R (nR)] for B tokens: z of the candidates (zc),
 // their scores, and the z planes of R.
+// The same from the gate/up slab of the current partition.
+pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st) {
+  GateUpSlabArgs a{};
+  a.slab = h->gu_slab;
+  a.geom = h->gu_geom;
+  a.D = h->D;
+  a.N = h->N;
+  a.B = B;
+  a.NP = round_up(B, 16);
+  a.rc = h->rc;
+  a.nC = h->cnt.n_C;
+  a.nR = h->cnt.n_R;
+  a.n2 = h->n2;
+  a.zc = h->z;
+  a.ldzc = round_up(B, 4);
+  a.zk = h->zk;
+  a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
+  a.ldk = h->ldk;
+  a.scores = h->scores;
+  a.err = h->err;
+  a.wait_ns = h->wait_ns;
+  CUtensorMap xm;
+  if (!encode_tokens_map(&xm, x, h->D, B, h->D, a.NP))
+    return fail(h, POP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed for x");
+  POP_CUDA(h, launch_gateup_slab(xm, a, h->num_sms, st));
+  return POP_OK;
+}
+
 pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st) {
   GateUpTcArgs a{};
   a.Wp = h->Wp;
@@ -209,6 +248,7 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.ldk = h->ldk;
   a.y = y;
   a.out_f32 = h->cfg.out_f32;
+  a.dslab = decode ? h->dn_slab : nullptr;
   a.sel = decode && h->cnt.n_C > 0 ? 1 : 0;
   a.scores = h->scores;
   a.zc = h->z;
@@ -345,6 +385,9 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   if (cfg->max_batch > 1) {
     POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
     POP_ALLOC(h->ch_s, N);
+    h->gu_geom = gu_slab_geom(cnt.n_C + cnt.n_R, D, h->num_sms);
+    POP_ALLOC(h->gu_slab, gu_slab_elems(h->gu_geom));
+    POP_ALLOC(h->dn_slab, dn_slab_elems(D, cnt.n_R));
   }
   POP_ALLOC(h->step, 1);
   POP_ALLOC(h->err, 1);
@@ -430,6 +473,7 @@ pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, voi
   POP_CUDA(h, launch_partition(h->sumsq, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step,
                                h->memory, h->err, st));
   POP_CUDA(h, reset_counters(h, st));
+  POP_CUDA(h, build_slabs(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -443,6 +487,7 @@ pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, v
   POP_CUDA(h, launch_partition(nullptr, h->n2, h->I, h->N, h->cnt.n_P, h->cnt.n_R, h->rc, h->P, h->step, h->memory,
                                h->err, st));
   POP_CUDA(h, reset_counters(h, st));
+  POP_CUDA(h, build_slabs(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -472,6 +517,7 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
   POP_CUDA(h, cudaMemsetAsync(h->step, 0, sizeof(int), st));
   POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
   POP_CUDA(h, reset_counters(h, st));
+  POP_CUDA(h, build_slabs(h, st));
   POP_CUDA(h, cudaStreamSynchronize(st));
   h->partitioned = true;
   h->selected = false;
@@ -507,7 +553,7 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
   } else {
     // gate/up, then the down GEMM over R and the selected items with the selection inside
     prof_mark(h, 0, st);
-    pop_status s = gateup_tc(h, static_cast<const uint16_t*>(x), B, h->rc, nC, nR, st);
+    pop_status s = gateup_slab(h, static_cast<const uint16_t*>(x), B, st);
     if (s != POP_OK) return s;
     prof_mark(h, 1, st);
     prof_mark(h, 2, st);

@@ -62,6 +62,7 @@ struct DownTcArgs {
   int ldk;
   void* y;               // out: [B][D], fp32 or bf16
   int out_f32;
+  const uint16_t* dslab; // down slab of R (units are then the 128-output slices of the slab), or NULL
   // selection by the first cluster (sel = 1, decode with candidates)
   int sel;
   const float* scores;   // [nC] this step's candidate scores
@@ -82,6 +83,44 @@ struct DownTcArgs {
 };
 // gate/up over R u C: z of the candidates, their scores, and the z planes of R
 cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int num_sms, cudaStream_t st);
+
+// ---- decode slabs for B > 1 (pop_decode_tc.cu): the weights a partition keeps, repacked once per
+// partition into tiles that are byte for byte the shared-memory operand images of the decode GEMMs,
+// so that decode streams them with one bulk copy per stage instead of gathering rows.
+// Gate/up slab: positions [0, P) of rc in T tiles of RT positions; tile t, k-block kb is an A tile of
+// `arows` rows x 128 bytes (128-byte swizzle) at ((t * KB + kb) * arows) * 64 elements. With RT <= 64
+// ("paired") gate and up of position j share one MMA: row 32 (j / 16) + 16 g + j % 16; otherwise the
+// gate rows fill rows [0, RT) and the up rows start at row round8(RT).
+struct GuSlabGeom {
+  int P, T, RT, KB, arows, paired;
+};
+GuSlabGeom gu_slab_geom(int P, int D, int num_sms);
+size_t gu_slab_elems(const GuSlabGeom& g);
+// Down slab: the down columns of R in tiles of 64 items x 128 outputs (MN-major image: two halves of
+// 64 outputs, 64 items x 128 bytes each, 128-byte swizzle) at ((o * kbr + b) * 8192) elements for
+// output slice o (of ceil(D / 128)) and item block b (of kbr = ceil(nR / 64)).
+size_t dn_slab_elems(int D, int nR);
+cudaError_t launch_build_slabs(const uint16_t* Wp, const int* rc, int nC, int nR, int D, int N, const GuSlabGeom& g,
+                               uint16_t* gu_slab, uint16_t* dn_slab, unsigned* err, cudaStream_t st);
+struct GateUpSlabArgs {
+  const uint16_t* slab;
+  GuSlabGeom geom;
+  int D, N;
+  int B, NP;
+  const int* rc;         // for the candidates' down-column norms
+  int nC, nR;
+  const float* n2;
+  float* zc;             // out, as GateUpTcArgs
+  int ldzc;
+  uint16_t* zk;
+  uint16_t* zk_lo;
+  int ldk;
+  float* scores;
+  int ks, stages;        // set by the launcher
+  unsigned* err;
+  uint64_t wait_ns;
+};
+cudaError_t launch_gateup_slab(const CUtensorMap& x_map, GateUpSlabArgs args, int num_sms, cudaStream_t st);
 // the selection (when args.sel), then y = sum over R and the selected items of z W2[:, channel]
 cudaError_t launch_down_tc(DownTcArgs args, int num_sms, cudaStream_t st);
 
