@@ -46,6 +46,16 @@ Readings where the pages are silent or garbled (each repeated at its function):
    memory M sums the aggregated candidate scores every step; at steps with
    t mod P == 0 the selection is redone from M and M is cleared; in between
    the last selection is held. P = 1 is per-step POP.
+7. MoE experts ([POP] "Loss / training strategy" applies the method to MoE
+   models with dynamic routing, taking the partition at the first forward,
+   but gives no routing rule): each token goes to its two largest router
+   logits (ties to the lower expert), weighted by the softmax over those two
+   logits. Each expert's partition comes from the prompt tokens routed to it;
+   an expert that gets none has s = 0, so I = 0 and the index tie rule alone
+   decides its split. Every decode step advances every expert's step counter
+   and memory; an expert that receives no token in a step scores each
+   candidate 0 (the maximum of non-negative values over no tokens) and
+   contributes no output.
 """
 from __future__ import annotations
 
@@ -56,7 +66,7 @@ import numpy as np
 __all__ = [
     "silu", "ffn_activations", "dense_ffn", "column_norms", "channel_importance", "RegionCounts",
     "region_counts", "partition", "candidate_scores", "select_topk", "down_projection", "prefill",
-    "PopSession", "moe_route",
+    "PopSession", "moe_route", "moe_prefill", "MoeSession",
 ]
 
 
@@ -183,6 +193,8 @@ def candidate_scores(Z_C, n2_C) -> np.ndarray:
     Z_C = _f64(Z_C)
     if Z_C.shape[1] == 0:
         return np.zeros(0)
+    if Z_C.shape[0] == 0:  # no token this step (an idle MoE expert, reading 7)
+        return np.zeros(Z_C.shape[1])
     return np.max(np.abs(Z_C), axis=0) * _f64(n2_C)
 
 
@@ -292,3 +304,74 @@ def moe_route(logits, top: int = 2):
     w = np.exp(sel - sel.max(axis=1, keepdims=True))
     w /= w.sum(axis=1, keepdims=True)
     return experts, w
+
+
+def _routed_tokens(experts, e: int) -> np.ndarray:
+    """Ascending indices of the tokens whose routing includes expert e."""
+    return np.nonzero(np.any(experts == e, axis=1))[0]
+
+
+def _combine(experts, weights, outputs, D: int) -> np.ndarray:
+    """y_t = sum over the token's routing choices j (in rank order) of w_{t,j} * (expert e_{t,j}'s output for t).
+
+    `outputs[e]` maps token index -> that expert's output row.
+    """
+    T = experts.shape[0]
+    Y = np.zeros((T, D))
+    for t in range(T):
+        for j in range(experts.shape[1]):
+            Y[t] += weights[t, j] * outputs[int(experts[t, j])][t]
+    return Y
+
+
+def moe_prefill(expert_weights, X, logits, r: float, gamma: float, top: int = 2):
+    """Prefill of an MoE layer of gated-MLP experts (reading 7).
+
+    expert_weights: list of (Wg, W1, W2) per expert; X [T, D]; logits [T, E].
+    Each expert runs `prefill` on its routed tokens (ascending token order) and
+    takes its partition from them; the layer output is the routing-weighted sum
+    of the experts' dense outputs. Returns dict(Y, experts, weights, parts) with
+    parts[e] = dict(R, C, P, I, counts, tokens).
+    """
+    X = _f64(X)
+    experts, weights = moe_route(logits, top)
+    D = X.shape[1]
+    outputs, parts = [], []
+    for e, (Wg, W1, W2) in enumerate(expert_weights):
+        tok = _routed_tokens(experts, e)
+        N = _f64(Wg).shape[0]
+        if tok.size:
+            pre = prefill(Wg, W1, W2, X[tok], r, gamma)
+            parts.append(dict(R=pre["R"], C=pre["C"], P=pre["P"], I=pre["I"], counts=pre["counts"], tokens=tok))
+            outputs.append({int(t): pre["Y"][row] for row, t in enumerate(tok)})
+        else:
+            counts = region_counts(N, r, gamma)
+            I = np.zeros(N)
+            R, C, P = partition(I, counts)
+            parts.append(dict(R=R, C=C, P=P, I=I, counts=counts, tokens=tok))
+            outputs.append({})
+    return dict(Y=_combine(experts, weights, outputs, D), experts=experts, weights=weights, parts=parts)
+
+
+@dataclass
+class MoeSession:
+    """Decode-time state of an MoE layer: one PopSession per expert (reading 7).
+
+    `step(x, logits)` routes the B tokens, runs every expert's decode step on the
+    tokens routed to it (possibly none) and combines the outputs.
+    """
+    sessions: list
+    top: int = 2
+    last_experts: np.ndarray = field(default=None)
+    last_weights: np.ndarray = field(default=None)
+
+    def step(self, x, logits) -> np.ndarray:
+        x = _f64(x)
+        experts, weights = moe_route(logits, self.top)
+        outputs = []
+        for e, sess in enumerate(self.sessions):
+            tok = _routed_tokens(experts, e)
+            ye = sess.step(x[tok])
+            outputs.append({int(t): ye[row] for row, t in enumerate(tok)})
+        self.last_experts, self.last_weights = experts, weights
+        return _combine(experts, weights, outputs, x.shape[1])

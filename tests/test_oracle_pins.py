@@ -358,3 +358,121 @@ def test_moe_route():
     np.testing.assert_allclose(w.sum(axis=1), 1.0)
     assert w[0, 0] == pytest.approx(0.5)
     assert w[1, 0] == pytest.approx(1.0 / (1.0 + math.exp(-2.0)))
+
+
+# ----------------------------------------------------------------- MoE experts (reading 7)
+
+def _moe_experts(E, D, N, same=False):
+    return [_tiny_layer(40 if same else 40 + e, D, N) for e in range(E)]
+
+
+def test_moe_route_against_pairwise_brute_force():
+    rng = np.random.default_rng(7)
+    L = np.round(rng.normal(size=(200, 6)), 1)  # one decimal: many exact ties
+    e, w = oracle.moe_route(L)
+    for t in range(L.shape[0]):
+        # brute force over ordered pairs (a, b), a != b: a beats every other expert, b every other but a;
+        # "beats" = larger logit, or equal logit and lower index
+        def beats(i, j):
+            return L[t, i] > L[t, j] or (L[t, i] == L[t, j] and i < j)
+        pairs = [(a, b) for a in range(6) for b in range(6) if a != b
+                 and all(beats(a, c) for c in range(6) if c != a)
+                 and all(beats(b, c) for c in range(6) if c not in (a, b))]
+        assert len(pairs) == 1 and tuple(e[t]) == pairs[0]
+        d = L[t, e[t, 1]] - L[t, e[t, 0]]
+        assert w[t, 0] == pytest.approx(1.0 / (1.0 + math.exp(d)), rel=1e-14)
+        assert w[t, 1] == pytest.approx(math.exp(d) / (1.0 + math.exp(d)), rel=1e-14)
+
+
+def test_moe_identical_dense_experts_are_the_dense_ffn():
+    # r = 0 keeps every channel; identical experts and weights summing to one give the plain FFN
+    D, N, E = 16, 40, 4
+    ex = _moe_experts(E, D, N, same=True)
+    X = _x(41, 12, D)
+    L = np.random.default_rng(1).normal(size=(12, E))
+    pre = oracle.moe_prefill(ex, X, L, r=0.0, gamma=0.1)
+    Wg, W1, W2 = ex[0]
+    np.testing.assert_allclose(pre["Y"], oracle.dense_ffn(Wg, W1, W2, X), rtol=1e-12, atol=1e-14)
+    sess = oracle.MoeSession([oracle.PopSession(*ex[e], pre["parts"][e]["R"], pre["parts"][e]["C"],
+                                                pre["parts"][e]["counts"].k) for e in range(E)])
+    for t in range(3):
+        x = _x(41, 5, D, step=t)
+        y = sess.step(x, np.random.default_rng(10 + t).normal(size=(5, E)))
+        np.testing.assert_allclose(y, oracle.dense_ffn(Wg, W1, W2, x), rtol=1e-12, atol=1e-14)
+
+
+def test_moe_two_identical_experts_equal_one_pruned_layer():
+    # E = 2 with top-2 routing sends every token to both experts, so each sees the whole prompt,
+    # takes the single-layer partition and selection, and the weights sum to one
+    D, N = 16, 64
+    ex = _moe_experts(2, D, N, same=True)
+    X = _x(42, 10, D)
+    L = np.random.default_rng(2).normal(size=(10, 2))
+    pre = oracle.moe_prefill(ex, X, L, r=0.3, gamma=0.1)
+    single = oracle.prefill(*ex[0], X, 0.3, 0.1)
+    for p in pre["parts"]:
+        for name in ("R", "C", "P"):
+            assert p[name].tolist() == single[name].tolist()
+    np.testing.assert_allclose(pre["Y"], single["Y"], rtol=1e-12, atol=1e-14)
+    moe = oracle.MoeSession([oracle.PopSession(*ex[e], single["R"], single["C"], single["counts"].k)
+                             for e in range(2)])
+    one = oracle.PopSession(*ex[0], single["R"], single["C"], single["counts"].k)
+    for t in range(4):
+        x = _x(42, 3, D, step=t)
+        np.testing.assert_allclose(moe.step(x, np.random.default_rng(20 + t).normal(size=(3, 2))), one.step(x),
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_moe_idle_expert_split_is_the_index_tie_rule():
+    # experts 2 and 3 never receive a token: s = 0, I = 0, so R is the n_R lowest indices, P the n_P
+    # highest, and every decode step selects the k lowest candidate positions (all scores 0)
+    D, N, E = 8, 30, 4
+    ex = _moe_experts(E, D, N)
+    X = _x(43, 9, D)
+    L = np.full((9, E), -5.0)
+    L[:, 0], L[:, 1] = 1.0, 0.5
+    pre = oracle.moe_prefill(ex, X, L, r=0.3, gamma=0.1)
+    c = oracle.region_counts(N, 0.3, 0.1)
+    for e in (2, 3):
+        p = pre["parts"][e]
+        assert p["tokens"].size == 0
+        assert p["R"].tolist() == list(range(c.n_R))
+        assert p["P"].tolist() == list(range(N - c.n_P, N))
+        assert p["C"].tolist() == list(range(c.n_R, N - c.n_P))
+    sess = [oracle.PopSession(*ex[e], pre["parts"][e]["R"], pre["parts"][e]["C"], pre["parts"][e]["counts"].k)
+            for e in range(E)]
+    moe = oracle.MoeSession(sess)
+    busy = [oracle.PopSession(*ex[e], pre["parts"][e]["R"], pre["parts"][e]["C"], pre["parts"][e]["counts"].k)
+            for e in range(2)]
+    for t in range(3):
+        x = _x(43, 4, D, step=t)
+        Lt = np.full((4, E), -5.0)
+        Lt[:, 0], Lt[:, 1] = 2.0, 1.0
+        y = moe.step(x, Lt)
+        w0 = 1.0 / (1.0 + math.exp(-1.0))
+        np.testing.assert_allclose(y, w0 * busy[0].step(x) + (1.0 - w0) * busy[1].step(x), rtol=1e-12, atol=1e-14)
+        for e in (2, 3):
+            assert sess[e].S.tolist() == list(range(c.k))
+            assert sess[e].t == t + 1
+
+
+def test_moe_token_permutation_permutes_outputs():
+    D, N, E = 16, 48, 4
+    ex = _moe_experts(E, D, N)
+    X = _x(44, 14, D)
+    L = np.random.default_rng(4).normal(size=(14, E))
+    perm = np.random.default_rng(5).permutation(14)
+    a = oracle.moe_prefill(ex, X, L, 0.3, 0.1)
+    b = oracle.moe_prefill(ex, X[perm], L[perm], 0.3, 0.1)
+    np.testing.assert_allclose(b["Y"], a["Y"][perm], rtol=1e-12, atol=1e-14)
+    for pa, pb in zip(a["parts"], b["parts"]):
+        for name in ("R", "C", "P"):
+            assert pa[name].tolist() == pb[name].tolist()
+    sa = oracle.MoeSession([oracle.PopSession(*ex[e], a["parts"][e]["R"], a["parts"][e]["C"],
+                                              a["parts"][e]["counts"].k) for e in range(E)])
+    sb = oracle.MoeSession([oracle.PopSession(*ex[e], a["parts"][e]["R"], a["parts"][e]["C"],
+                                              a["parts"][e]["counts"].k) for e in range(E)])
+    x = _x(44, 6, D, step=0)
+    Lt = np.random.default_rng(6).normal(size=(6, E))
+    q = np.random.default_rng(7).permutation(6)
+    np.testing.assert_allclose(sb.step(x[q], Lt[q]), sa.step(x, Lt)[q], rtol=1e-12, atol=1e-14)
