@@ -44,6 +44,9 @@ WORKLOADS = {
                               chunk=4096),
     "llama-70b-ffn-b64-p16": dict(D=8192, N=28672, r=0.5, gamma=0.1, B=64, M=64 * 512, T=1024, period=16,
                                   layers=1, chunk=8192),
+    # MoE layer: 8 experts of D=4096, D_FF=14336, top-2 routing, prompt of 8 sequences x 512 tokens
+    "moe-8x4096x14336-b32": dict(D=4096, N=14336, r=0.3, gamma=0.1, B=32, M=8 * 512, T=128, period=1, layers=1,
+                                 chunk=2048, experts=8),
 }
 METRIC = "pruned-FFN decode tokens/s and HBM GB/s vs GB300 peak, LLaMA-7B FFN, B=1/16"
 # Per-kernel durations come from a separate pass after the timed region in which every decode step
@@ -161,6 +164,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm
 
+def prefill_launches(chunks, max_batch):
+    return 3 * chunks + 1 + (2 if max_batch > 1 else 0)
+
+
+def decode_launches(c, B):
+    return (2 + (1 if c.n_C > 8192 else 0)) if B == 1 else 2
+
+
 class Stack:
     """`layers` independent POP FFN layers of one workload, with their inputs resident in HBM."""
 
@@ -200,12 +211,12 @@ class Stack:
         self.chunks = (M + wl["chunk"] - 1) // wl["chunk"]
 
     def launches_per_session(self):
-        # prefill: per chunk gate/up GEMM + sum fold + down GEMM, then the partition kernel;
-        # decode at B = 1: gate/up with the top-k inside (+ a separate top-k when |C| > 8192) and the
-        # tiled down projection; at B > 1: gate/up with the selection inside, and the down GEMM
-        c = self.counts
-        per_step = (2 + (1 if c.n_C > 8192 else 0)) if self.wl["B"] == 1 else 2
-        per_layer = 3 * self.chunks + 1 + per_step * self.wl["T"]
+        # prefill: per chunk gate/up GEMM + sum fold + down GEMM, then the partition kernel (and at
+        # B > 1 the two slab builders); decode at B = 1: gate/up with the top-k inside (+ a separate
+        # top-k when |C| > 8192) and the tiled down projection; at B > 1: the gate/up GEMM, then the
+        # down GEMM with the selection inside
+        per_layer = prefill_launches(self.chunks, self.wl["B"]) + decode_launches(self.counts, self.wl["B"]) * \
+            self.wl["T"]
         return per_layer * self.wl["layers"]
 
     def session(self, dec_events=None):
@@ -255,11 +266,117 @@ class Stack:
             f.close()
 
 
+class MoeStack:
+    """One MoE layer (top-2 routing over `experts` POP-pruned experts) with its inputs resident in HBM."""
+
+    def __init__(self, wl, seed=0):
+        import numpy as np
+        import torch
+
+        import online_structured_ffn_gb300 as pop
+        import synth
+        self.wl, self.pop, self.torch = wl, pop, torch
+        dev = torch.device("cuda", torch.cuda.current_device())
+        D, N, B, M, T, E = wl["D"], wl["N"], wl["B"], wl["M"], wl["T"], wl["experts"]
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def f32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+        ws = [[], [], []]
+        for e in range(E):
+            for i, w in enumerate(synth.ffn_weights(seed, D, N, layer=e)):
+                ws[i].append(up(w))
+        self.moe = pop.PopMoE(ws[0], ws[1], ws[2], r=wl["r"], gamma=wl["gamma"], period=wl["period"], max_batch=B,
+                              max_prefill_tokens=wl["chunk"], out_f32=True)
+        torch.cuda.synchronize()
+        del ws
+        self.ffn = self.moe.experts
+        self.counts = self.moe.counts
+        sc = synth.dim_scales(seed, D)
+        self.X = [up(synth.prompt(seed, M, sc))]
+        self.Lp = f32(synth.router_logits(seed, M, E))
+        self.Y = [torch.empty((M, D), dtype=torch.float32, device=dev)]
+        self.x = up(np.stack([synth.decode_input(seed, t, B, sc)[None] for t in range(T)]))  # [T, 1, B, D]
+        self.L = f32(np.stack([synth.router_logits(seed, B, E, step=t) for t in range(T)]))  # [T, B, E]
+        self.y = torch.empty((T, 1, B, D), dtype=torch.float32, device=dev)
+        # route the prompt once, so the experts' token counts (and the launch count) are known
+        self.moe.prefill_partition(self.X[0], self.Lp, self.Y[0])
+        self.prompt_counts = self.moe.token_counts()
+
+    def launches_per_session(self):
+        import numpy as np
+        wl = self.wl
+        E = wl["experts"]
+        n = 3 + 1  # route top-2, token slots, gather; combine
+        for c in self.prompt_counts:
+            n += prefill_launches(int(np.ceil(c / wl["chunk"])), wl["B"]) if c else 1 + (2 if wl["B"] > 1 else 0)
+        n += wl["T"] * (2 + E * decode_launches(self.counts, wl["B"]))
+        return n
+
+    def session(self, dec_events=None):
+        pop, torch = self.pop, self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        B, T, D, E = self.wl["B"], self.wl["T"], self.wl["D"], self.wl["experts"]
+        lib = pop.load_library()
+        h = self.moe.handle
+        s = lib.pop_moe_prefill_partition(h, self.X[0].data_ptr(), self.Lp.data_ptr(), self.X[0].shape[0],
+                                          self.Y[0].data_ptr(), st)
+        if s:
+            pop._check_moe(s, h)
+        if dec_events is not None:
+            dec_events[0].record()
+        xp, lp, yp = self.x.data_ptr(), self.L.data_ptr(), self.y.data_ptr()
+        for t in range(T):
+            s = lib.pop_moe_decode_step(h, xp + t * B * D * 2, lp + t * B * E * 4, B, yp + t * B * D * 4, st)
+            if s:
+                pop._check_moe(s, h)
+        if dec_events is not None:
+            dec_events[1].record()
+
+    def session_e2e(self, hX, hx, hY, hy):
+        pop, torch = self.pop, self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        B, T = self.wl["B"], self.wl["T"]
+        self.X[0].copy_(hX[0], non_blocking=True)
+        self.Lp.copy_(self.hLp, non_blocking=True)
+        self.moe.prefill_partition(self.X[0], self.Lp, self.Y[0])
+        hY[0].copy_(self.Y[0], non_blocking=True)
+        lib = pop.load_library()
+        for t in range(T):
+            self.x[t].copy_(hx[t], non_blocking=True)
+            self.L[t].copy_(self.hL[t], non_blocking=True)
+            s = lib.pop_moe_decode_step(self.moe.handle, self.x[t].data_ptr(), self.L[t].data_ptr(), B,
+                                        self.y[t].data_ptr(), st)
+            if s:
+                pop._check_moe(s, self.moe.handle)
+            hy[t].copy_(self.y[t], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def e2e_extra_h2d(self):
+        """Pinned host copies of the router logits; returns their bytes per session."""
+        self.hLp = self.Lp.cpu().pin_memory()
+        self.hL = self.L.cpu().pin_memory()
+        return self.hLp.numel() * 4 + self.hL.numel() * 4
+
+    def check(self):
+        self.moe.check()
+
+    def close(self):
+        self.moe.close()
+
+
+def make_stack(wl):
+    return MoeStack(wl) if wl.get("experts") else Stack(wl)
+
+
 def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     import torch
     wl = WORKLOADS[wl_name]
     rank, world, local = dist_info()
-    stack = Stack(wl)
+    stack = make_stack(wl)
     for f in stack.ffn:
         f.check()
     for _ in range(warmup):
@@ -282,6 +399,8 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     barrier()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     dec_s = sum(a.elapsed_time(b) for a, b in dec) / 1e3
+    if hasattr(stack, "check"):
+        stack.check()
     for f in stack.ffn:
         f.check()
     # profiled pass: the same sessions with events between the kernels of every decode step
@@ -301,6 +420,7 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     nsteps = sum(p[1] for p in prof)
     c = stack.counts
     gu_bytes, dn_bytes = touched_bytes(c, wl["D"])
+    nexp = wl.get("experts", 1)  # every expert streams its weights every step
     peak, peak_kind = measured_peaks()
     gu_ms = ksum[0] / max(nsteps, 1)
     roof_bytes = gu_bytes
@@ -314,7 +434,7 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
         roof_bytes=roof_bytes,
         gateup_gbs=roof_bytes / (gu_ms * 1e-3) / 1e9,
         peak=peak, peak_kind=peak_kind,
-        step_gbs=(gu_bytes + dn_bytes) / dec_step_s / 1e9,
+        step_gbs=nexp * (gu_bytes + dn_bytes) / dec_step_s / 1e9, experts=nexp,
         gu_bytes=gu_bytes, dn_bytes=dn_bytes, counts=c.as_dict(),
         launches=stack.launches_per_session() * steps,
         clocks=sampler.summary() if sampler else None,
@@ -334,6 +454,7 @@ def run_e2e(stack, steps):
     hY = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in stack.Y]
     hx = stack.x.cpu().pin_memory()
     hy = torch.empty(stack.y.shape, dtype=stack.y.dtype).pin_memory()
+    extra = stack.e2e_extra_h2d() if hasattr(stack, "e2e_extra_h2d") else 0
     stack.session_e2e(hX, hx, hY, hy)  # warm
     barrier()
     torch.cuda.synchronize()
@@ -345,7 +466,7 @@ def run_e2e(stack, steps):
     barrier()
     units = wl["B"] * wl["T"] * wl["layers"] * steps
     g_el, g_units = aggregate(el, units, device=torch.device("cuda", torch.cuda.current_device()))
-    h2d = sum(x.numel() * x.element_size() for x in hX) + hx.numel() * hx.element_size()
+    h2d = sum(x.numel() * x.element_size() for x in hX) + hx.numel() * hx.element_size() + extra
     d2h = sum(y.numel() * y.element_size() for y in hY) + hy.numel() * hy.element_size()
     return {"value": g_units / g_el, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps}
@@ -364,10 +485,15 @@ class OracleSample:
         self.wl, self.oracle = wl, oracle
         f64 = synth.bf16_to_f64
         D, N, B = wl["D"], wl["N"], wl["B"]
+        self.E = wl.get("experts", 1)
+        # an MoE layer is sampled through one expert: its expected share of the tokens (2 of E
+        # experts per token), extrapolated to all E experts
+        self.share = 2.0 / self.E if self.E > 1 else 1.0
+        self.Bs = max(1, int(round(B * self.share)))
         self.W = tuple(f64(w) for w in synth.ffn_weights(seed, D, N))
         sc = synth.dim_scales(seed, D)
         self.X = f64(synth.prompt(seed, max_prefill, sc))
-        self.xs = [f64(synth.decode_input(seed, t, B, sc)) for t in range(max_decode)]
+        self.xs = [f64(synth.decode_input(seed, t, self.Bs, sc)) for t in range(max_decode)]
 
     def run(self, prefill_tokens, decode_steps):
         wl, oracle = self.wl, self.oracle
@@ -380,10 +506,16 @@ class OracleSample:
         for x in self.xs[:decode_steps]:
             sess.step(x)
         t_dec = (time.perf_counter() - t0) / decode_steps
-        session = t_pre * wl["M"] / prefill_tokens + t_dec * wl["T"]
-        info = (f"one layer of the {wl['D']}x{wl['N']} FFN: oracle prefill of {prefill_tokens} of {wl['M']} "
-                f"prompt tokens ({t_pre:.2f} s) and {decode_steps} of {wl['T']} decode steps at B={wl['B']} "
-                f"({t_dec:.2f} s each), extrapolated linearly to one full session")
+        session = self.E * (t_pre * wl["M"] * self.share / prefill_tokens + t_dec * wl["T"])
+        if self.E > 1:
+            info = (f"one of {self.E} experts ({wl['D']}x{wl['N']}) of the MoE layer: oracle prefill of "
+                    f"{prefill_tokens} of its ~{wl['M'] * self.share:.0f} routed prompt tokens ({t_pre:.2f} s) and "
+                    f"{decode_steps} of {wl['T']} decode steps at its ~{self.Bs} routed tokens ({t_dec:.2f} s each), "
+                    f"extrapolated linearly to one full session of all {self.E} experts")
+        else:
+            info = (f"one layer of the {wl['D']}x{wl['N']} FFN: oracle prefill of {prefill_tokens} of {wl['M']} "
+                    f"prompt tokens ({t_pre:.2f} s) and {decode_steps} of {wl['T']} decode steps at B={wl['B']} "
+                    f"({t_dec:.2f} s each), extrapolated linearly to one full session")
         return session, info
 
 
@@ -402,17 +534,27 @@ def cpu_baseline(wl):
 
 # ------------------------------------------------------------------ main
 
-def traffic_from_profiles(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+def code_hash(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a source file's code: comments and blank lines are
+    dropped, so that editing a comment does not retire a profile of unchanged code."""
     import hashlib
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current code."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     src_name = "pop_decode1.cu" if workload.endswith("-b1") else "pop_decode_tc.cu"
-    src = open(os.path.join(ROOT, "online_structured_ffn_gb300", "csrc", src_name), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
+    sha = code_hash(os.path.join(ROOT, "online_structured_ffn_gb300", "csrc", src_name))
     vals = {}
     for line in text.splitlines():
         line = line.strip().lstrip("-* ")
@@ -436,8 +578,12 @@ def main():
     ap.add_argument("--workload", default="llama2-7b-ffn-b1", choices=sorted(WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true", help="skip the B=16 line inside the JSON")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="override the workload's decode steps per session (short runs for profiler captures)")
     args = ap.parse_args()
     rank, world, local = dist_info()
+    if args.decode_steps > 0:
+        WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], T=args.decode_steps)
     wl = WORKLOADS[args.workload]
     config = {"workload": args.workload, "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
               "B": wl["B"], "prompt_tokens": wl["M"], "decode_steps": wl["T"], "period": wl["period"],
@@ -501,12 +647,14 @@ def main():
         "config": config,
         "roofline": {"bound": "hbm",
                      "kernel": ("k_gateup_sel_b1 (decode gate/up over R u C, top-k inside)" if wl["B"] == 1
-                                else "k_gateup_tc (decode gate/up over R u C on tcgen05, top-k inside, B > 1)"),
+                                else "k_gateup_slab (decode gate/up over R u C on tcgen05 from the partition's "
+                                     "weight slab, B > 1)"),
                      "achieved": res["gateup_gbs"], "peak": res["peak"], "unit": "GB/s",
                      "frac": res["gateup_gbs"] / res["peak"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": res["roof_bytes"], "peak_source": res["peak_kind"]},
         "decode_step": {"us": res["decode_step_us"], "hbm_gbs": res["step_gbs"], "frac": res["step_gbs"] / res["peak"],
-                        "touched_bytes": res["gu_bytes"] + res["dn_bytes"], "kernel_us": res["kernel_us"],
+                        "touched_bytes": res["experts"] * (res["gu_bytes"] + res["dn_bytes"]),
+                        "kernel_us": res["kernel_us"],
                         "tokens_per_s": res["decode_only_tokens_per_s"]},
         "prefill_ms_per_layer": res["prefill_ms_per_layer"],
         "counts": res["counts"],

@@ -128,9 +128,11 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
  * Computes z over R u C, candidate scores a_i = max_b |z_{b,i}| * ||W2[:,i]||, updates the memory,
  * selects the k best candidates when step % period == 0 (ties to the lower index), and writes
  * y = sum over R u S of z_i * W2[:,i]. No allocation and no host synchronization. The step is two
- * kernels launched with programmatic dependent launch (gate/up with the selection inside, then the
- * down projection; the next kernel's weight loads overlap the previous kernel's tail); each waits
- * for its predecessor before it touches data a previous call may still use.
+ * kernels launched with programmatic dependent launch (gate/up, then the down projection; the
+ * selection runs inside the gate/up kernel at B = 1 and inside the down kernel at B > 1, and at
+ * B = 1 with |C| > 8192 as a third kernel between them). The next kernel's weight loads overlap
+ * the previous kernel's tail; each kernel waits for its predecessor before it touches data a
+ * previous call may still use.
  * STATE if no partition has been set. */
 pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* stream);
 

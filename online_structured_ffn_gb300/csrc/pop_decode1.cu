@@ -126,10 +126,12 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
   // ------------------------------------------------------------------ workers
   const int W = G - 1, j = cta - 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cb0 = static_cast<int>(static_cast<long long>(j) * a.nC / W);
-  const int cb1 = static_cast<int>(static_cast<long long>(j + 1) * a.nC / W);
-  const int rb0 = a.nC + static_cast<int>(static_cast<long long>(j) * a.nR / W);
-  const int rb1 = a.nC + static_cast<int>(static_cast<long long>(j + 1) * a.nR / W);
+  // 32-bit splits (the launcher checks that the products fit): 64-bit division is slow here
+  const unsigned uW = static_cast<unsigned>(W), uj = static_cast<unsigned>(j);
+  const int cb0 = static_cast<int>(uj * static_cast<unsigned>(a.nC) / uW);
+  const int cb1 = static_cast<int>((uj + 1u) * static_cast<unsigned>(a.nC) / uW);
+  const int rb0 = a.nC + static_cast<int>(uj * static_cast<unsigned>(a.nR) / uW);
+  const int rb1 = a.nC + static_cast<int>((uj + 1u) * static_cast<unsigned>(a.nR) / uW);
   const int c0 = cb0 + warp * (cb1 - cb0) / GS_WARPS, c1 = cb0 + (warp + 1) * (cb1 - cb0) / GS_WARPS;
   const int r0 = rb0 + warp * (rb1 - rb0) / GS_WARPS, r1 = rb0 + (warp + 1) * (rb1 - rb0) / GS_WARPS;
   const int nch = D >> 3;
@@ -229,10 +231,11 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   const bool dok = d < D;
   // chunk c takes the c-th share of R and the c-th share of S, so every CTA has the same mix of
   // prefetched (R) and not prefetched (S) columns
-  const int r_lo = static_cast<int>(static_cast<long long>(chunk) * a.nR / NCK);
-  const int nr = static_cast<int>(static_cast<long long>(chunk + 1) * a.nR / NCK) - r_lo;
-  const int s_lo = static_cast<int>(static_cast<long long>(chunk) * a.kd / NCK);
-  const int ns = static_cast<int>(static_cast<long long>(chunk + 1) * a.kd / NCK) - s_lo;
+  const unsigned uc = static_cast<unsigned>(chunk), un = static_cast<unsigned>(NCK);
+  const int r_lo = static_cast<int>(uc * static_cast<unsigned>(a.nR) / un);
+  const int nr = static_cast<int>((uc + 1u) * static_cast<unsigned>(a.nR) / un) - r_lo;
+  const int s_lo = static_cast<int>(uc * static_cast<unsigned>(a.kd) / un);
+  const int ns = static_cast<int>((uc + 1u) * static_cast<unsigned>(a.kd) / un) - s_lo;
   const int n_items = nr + ns;  // item e < nr is R item r_lo + e, else S item s_lo + e - nr
   const size_t row3 = 3 * static_cast<size_t>(D);
   const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(D);  // down part of packed row 0
@@ -365,7 +368,11 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// the kernels split work with 32-bit products (part index x item count)
+static bool split_fits(long long parts, long long items) { return parts * items < (1LL << 32); }
+
 cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st) {
+  if (!split_fits(grid, a.nC > a.nR ? a.nC : a.nR)) return cudaErrorInvalidValue;
   const int nchl = pow2_ceil((a.D / 8 + 31) / 32);
   const size_t keys = a.do_select ? static_cast<size_t>(a.nC > 0 ? a.nC : 1) * sizeof(uint32_t) : 0;
   const size_t xsz = static_cast<size_t>(a.D) * sizeof(float);
@@ -401,6 +408,7 @@ int down_tiled_chunks(int D, int nitems, int num_sms) {
 cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st) {
   const int tiles = (a.D + DT_TILE - 1) / DT_TILE;
   const int nck = down_tiled_chunks(a.D, a.nR + a.kd, num_sms);
+  if (!split_fits(nck, a.nR > a.kd ? a.nR : a.kd)) return cudaErrorInvalidValue;
   return launch_pdl(k_down_tiled_b1, dim3(tiles, nck), dim3(DT_THREADS), 0, st, a);
 }
 

@@ -13,16 +13,20 @@
 // the two halves, which leaves z's own fp32 rounding well below the output tolerance.
 //
 // Both are skinny GEMMs with the tokens as the MMA's N (16..64, zero-padded to a multiple of 16)
-// and 128 rows as M. Eight producer warps gather the pruned weight rows straight from the packed
-// weights with 16-byte cp.async copies into the 128-byte swizzle layout (no copy of the pruned
-// weights is ever made). Measured on this part: the gather reaches ~6.2 TB/s with eight producer
-// warps against ~2-4 TB/s with two, and an MMA of M = 128, K = 16 costs ~44 cycles for N <= 32
-// whatever its rows hold, so each MMA should carry as many real rows as it can. A copy's landing
-// arrives on its stage's barrier by itself (cp.async.mbarrier.arrive), so a producer only ever
-// waits for a free slot; the MMA thread fences the landed copies for the tensor cores after its
-// barrier wait.
+// and 128 rows as M. The partition is fixed for a whole decode session, so each partition gets two
+// slabs, built once per prefill (k_build_gu_slab, k_build_dn_slab): the gate/up rows of R u C and
+// the down columns of R, copied from the packed weights into the exact shared-memory images the
+// MMAs read (pre-tiled and pre-swizzled). A decode stage is then one contiguous bulk copy of 16-72
+// KB, which streams at 6.7-7.2 TB/s, where gathering 128-512-byte row pieces with cp.async reached
+// 4.7-6.2 TB/s. The selected candidates change every step, so their down columns are still
+// gathered from the packed weights. Measured on this part: an MMA of M = 128, K = 16 costs ~44
+// cycles for N <= 32 whatever its rows hold, so each MMA should carry as many real rows as it can.
+// In the gathers a copy's landing arrives on its stage's barrier by itself
+// (cp.async.mbarrier.arrive), so a producer only ever waits for a free slot; the MMA thread fences
+// the landed copies for the tensor cores after its barrier wait.
 //
-// Gate/up (k_gateup_tc): one CTA per SM; each CTA streams "units" of at most 64 positions over all
+// Gate/up by gathering (k_gateup_tc, used by the dense reference path at B > 1, where every
+// channel is kept and no slab exists): one CTA per SM; each CTA streams "units" of at most 64 positions over all
 // of K. The unit ranges are ragged (P / units each) so that the number of units matches the number
 // of CTAs. One MMA covers gate and up of a unit together: TMEM lane quarter q holds gate rows
 // 16q..16q+15 in lanes 0-15 and the up rows of the same positions in lanes 16-31, so an epilogue
@@ -34,7 +38,9 @@
 // previous kernel.
 //
 // Down (k_down_tc): each unit (at most 128 outputs) is split along K over a cluster of `split`
-// CTAs; every CTA streams its share of the R items first, then its share of the selected items.
+// CTAs; every CTA streams its share of the R items first (bulk copies from the down slab in the
+// decode, gathered columns in the dense reference path), then gathers its share of the selected
+// items.
 // The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
 // writes the selected channels and their z planes, and releases a flag; the other CTAs wait
 // (bounded) for the flag only when they reach their first selected item. The partial accumulators
