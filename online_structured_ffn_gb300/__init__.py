@@ -66,6 +66,18 @@ SIGNATURES = {
     "pop_check": (_i32, [_vp]),
     "pop_last_error": (ctypes.c_char_p, [_vp]),
     "pop_status_string": (ctypes.c_char_p, [_i32]),
+    # MoE layer (include/pop_moe.h)
+    "pop_moe_create": (_i32, [ctypes.POINTER(pop_config), _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                              ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp)]),
+    "pop_moe_destroy": (None, [_vp]),
+    "pop_moe_prefill_partition": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp]),
+    "pop_moe_decode_step": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp]),
+    "pop_moe_get_routing": (_i32, [_vp, _ip, _ip, _fp]),
+    "pop_moe_get_counts": (_i32, [_vp, _ip]),
+    "pop_moe_expert": (_vp, [_vp, _i32]),
+    "pop_moe_num_experts": (_i32, [_vp]),
+    "pop_moe_check": (_i32, [_vp]),
+    "pop_moe_last_error": (ctypes.c_char_p, [_vp]),
 }
 
 _lib = None
@@ -96,6 +108,12 @@ def status_name(s: int) -> str:
 def _check(status: int, handle=None):
     if status != POP_OK:
         msg = load_library().pop_last_error(handle)
+        raise PopError(status, msg.decode() if msg else "")
+
+
+def _check_moe(status: int, handle=None):
+    if status != POP_OK:
+        msg = load_library().pop_moe_last_error(handle)
         raise PopError(status, msg.decode() if msg else "")
 
 
@@ -250,7 +268,8 @@ class PopFFN:
 
     def close(self):
         if getattr(self, "handle", None):
-            pop_ffn_destroy(self.handle)
+            if not getattr(self, "_borrowed", False):
+                pop_ffn_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -312,6 +331,94 @@ class PopFFN:
 
     def check(self):
         pop_check(self.handle)
+
+    @classmethod
+    def _borrow(cls, handle, cfg):
+        """A view of a layer handle owned elsewhere (an MoE expert): close() leaves it alone."""
+        v = cls.__new__(cls)
+        v.cfg, v.D, v.N, v.handle, v._borrowed = cfg, cfg.D, cfg.D_FF, handle, True
+        v.counts = pop_ffn_counts(handle)
+        return v
+
+
+# ------------------------------------------------------------------ MoE layer
+
+def pop_moe_create(cfg: pop_config, Wg, W1, W2, stream=None) -> int:
+    E = len(Wg)
+    arr = [(_vp * E)(*[_ptr(w) for w in ws]) for ws in (Wg, W1, W2)]
+    out = _vp()
+    _check_moe(load_library().pop_moe_create(ctypes.byref(cfg), E, arr[0], arr[1], arr[2], _stream(stream),
+                                             ctypes.byref(out)))
+    return out.value
+
+
+class PopMoE:
+    """An MoE layer of POP-pruned gated-MLP experts (top-2 routing), backed by a pop_moe handle.
+
+    Wg, W1: lists of torch bf16 [D_FF, D] (one per expert); W2: list of bf16 [D, D_FF].
+    """
+
+    def __init__(self, Wg, W1, W2, r: float, gamma: float = 0.1, period: int = 1, max_batch: int = 1,
+                 max_prefill_tokens: int = 2048, out_f32: bool = True, stream=None):
+        N, D = Wg[0].shape
+        self.handle = None
+        self.cfg = pop_config(D=D, D_FF=N, r=r, gamma=gamma, period=period, max_batch=max_batch,
+                              max_prefill_tokens=max_prefill_tokens, out_f32=1 if out_f32 else 0)
+        self.D, self.N, self.E = D, N, len(Wg)
+        self.handle = pop_moe_create(self.cfg, Wg, W1, W2, stream)
+        self.experts = [PopFFN._borrow(load_library().pop_moe_expert(self.handle, e), self.cfg)
+                        for e in range(self.E)]
+        self.counts = self.experts[0].counts
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.experts = []
+            load_library().pop_moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.cfg.out_f32 else torch.bfloat16
+
+    def prefill_partition(self, X, logits, Y=None, stream=None):
+        """X: bf16 [M, D]; logits: float32 [M, E]; Y (optional): [M, D] of out_dtype()."""
+        _check_moe(load_library().pop_moe_prefill_partition(self.handle, _ptr(X), _ptr(logits), X.shape[0], _ptr(Y),
+                                                            _stream(stream)), self.handle)
+
+    def decode_step(self, x, logits, y=None, stream=None):
+        import torch
+        if y is None:
+            y = torch.empty((x.shape[0], self.D), dtype=self.out_dtype(), device=x.device)
+        _check_moe(load_library().pop_moe_decode_step(self.handle, _ptr(x), _ptr(logits), x.shape[0], _ptr(y),
+                                                      _stream(stream)), self.handle)
+        return y
+
+    def routing(self):
+        """(experts [T, 2] int32, weights [T, 2] float32) of the last call. Syncs."""
+        import numpy as np
+        lib = load_library()
+        T = ctypes.c_int(0)
+        _check_moe(lib.pop_moe_get_routing(self.handle, ctypes.byref(T), None, None), self.handle)
+        ex = np.zeros((max(T.value, 1), 2), dtype=np.int32)
+        w = np.zeros((max(T.value, 1), 2), dtype=np.float32)
+        _check_moe(lib.pop_moe_get_routing(self.handle, ctypes.byref(T), ex.ctypes.data_as(_ip),
+                                           w.ctypes.data_as(_fp)), self.handle)
+        return ex[:T.value], w[:T.value]
+
+    def token_counts(self):
+        import numpy as np
+        c = np.zeros(self.E, dtype=np.int32)
+        _check_moe(load_library().pop_moe_get_counts(self.handle, c.ctypes.data_as(_ip)), self.handle)
+        return c
+
+    def check(self):
+        _check_moe(load_library().pop_moe_check(self.handle), self.handle)
 
 
 load_library()

@@ -66,7 +66,7 @@ import numpy as np
 __all__ = [
     "silu", "ffn_activations", "dense_ffn", "column_norms", "channel_importance", "RegionCounts",
     "region_counts", "partition", "candidate_scores", "select_topk", "down_projection", "prefill",
-    "PopSession", "moe_route", "moe_prefill", "MoeSession",
+    "PopSession", "moe_route", "moe_prefill", "MoeSession", "moe_decode",
 ]
 
 
@@ -375,3 +375,31 @@ class MoeSession:
             outputs.append({int(t): ye[row] for row, t in enumerate(tok)})
         self.last_experts, self.last_weights = experts, weights
         return _combine(experts, weights, outputs, x.shape[1])
+
+
+def moe_decode(expert_weights, parts, xs, logits, k: int, period: int = 1, top: int = 2):
+    """The decode steps of an MoE layer, expert by expert (the same results as MoeSession.step).
+
+    expert_weights(e) -> (Wg, W1, W2) loads one expert's weights, so that only one expert's float64
+    copy is alive at a time; parts[e] = dict(R, C) is its partition; xs[t] [B, D] and logits[t]
+    [B, E] are the steps' inputs. The experts' steps are independent of one another, so running
+    each expert through all steps before the next gives the same outputs as stepping the layer.
+    Returns (ys [T, B, D], per_expert) with per_expert[e] = list over steps of dict(S, scores, C).
+    """
+    T = len(xs)
+    routes = [moe_route(l, top) for l in logits]
+    outputs = [[] for _ in range(T)]
+    per_expert = []
+    for e, part in enumerate(parts):
+        sess = PopSession(*expert_weights(e), part["R"], part["C"], k, period=period)
+        steps = []
+        for t in range(T):
+            tok = _routed_tokens(routes[t][0], e)
+            ye = sess.step(_f64(xs[t])[tok])
+            outputs[t].append({int(tt): ye[row] for row, tt in enumerate(tok)})
+            steps.append(dict(S=sess.C[sess.S], scores=sess.last_scores, C=sess.C))
+        per_expert.append(steps)
+        del sess
+    D = _f64(xs[0]).shape[1]
+    ys = np.stack([_combine(routes[t][0], routes[t][1], outputs[t], D) for t in range(T)])
+    return ys, per_expert

@@ -1,4 +1,4 @@
-"""The C-ABI library without a GPU: it loads, exports every symbol include/pop_ffn.h declares,
+"""The C-ABI library without a GPU: it loads, exports every symbol include/*.h declares,
 and its host-side logic (region counts, argument checks) agrees with the oracle."""
 import ctypes
 import os
@@ -20,7 +20,8 @@ def pop():
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "pop_ffn.h")).read()
+    inc = os.path.join(ROOT, "include")
+    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pop_[a-z_]+)\s*\(", text)))
 
@@ -30,7 +31,7 @@ def test_every_declared_symbol_is_exported(pop):
     assert len(names) >= 18
     lib = ctypes.CDLL(pop.LIB_PATH)
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in pop_ffn.h but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
     assert set(names) == set(pop.SIGNATURES), "binding and header disagree"
 
 
@@ -95,3 +96,40 @@ def test_status_strings(pop):
     for s in range(8):
         assert lib.pop_status_string(s).decode() == pop.status_name(s)
     assert lib.pop_status_string(99) == b"POP_ERR_UNKNOWN"
+
+
+def test_moe_rejects_bad_arguments_before_touching_cuda(pop):
+    lib = pop.load_library()
+    out = ctypes.c_void_p(1)
+    fake = 4096
+    good = dict(D=256, D_FF=1024, r=0.3, gamma=0.1, period=1, max_batch=4, max_prefill_tokens=64, out_f32=1)
+    cfg = pop.pop_config(**good)
+
+    def ptrs(n, v=fake):
+        return (ctypes.c_void_p * n)(*([v] * n))
+
+    for E in (0, 1, 257):
+        n = max(E, 1)
+        assert lib.pop_moe_create(ctypes.byref(cfg), E, ptrs(n), ptrs(n), ptrs(n), None, ctypes.byref(out)) == \
+            pop.POP_ERR_INVALID_ARG
+        assert out.value is None
+    assert lib.pop_moe_create(ctypes.byref(cfg), 2, None, ptrs(2), ptrs(2), None, ctypes.byref(out)) == \
+        pop.POP_ERR_INVALID_ARG
+    holes = (ctypes.c_void_p * 2)(fake, None)
+    assert lib.pop_moe_create(ctypes.byref(cfg), 2, ptrs(2), holes, ptrs(2), None, ctypes.byref(out)) == \
+        pop.POP_ERR_INVALID_ARG
+    bad = pop.pop_config(**{**good, "D": 100})  # rejected by the first expert's create, before CUDA
+    assert lib.pop_moe_create(ctypes.byref(bad), 2, ptrs(2), ptrs(2), ptrs(2), None, ctypes.byref(out)) == \
+        pop.POP_ERR_INVALID_ARG
+    assert b"expert 0" in lib.pop_moe_last_error(None)
+    assert lib.pop_moe_create(ctypes.byref(cfg), 2, ptrs(2), ptrs(2), ptrs(2), None, None) == pop.POP_ERR_INVALID_ARG
+    # NULL handles
+    assert lib.pop_moe_prefill_partition(None, fake, fake, 1, None, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_moe_decode_step(None, fake, fake, 1, fake, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_moe_check(None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_moe_get_counts(None, None) == pop.POP_ERR_INVALID_ARG
+    T = ctypes.c_int(0)
+    assert lib.pop_moe_get_routing(None, ctypes.byref(T), None, None) == pop.POP_ERR_INVALID_ARG
+    assert lib.pop_moe_expert(None, 0) is None
+    assert lib.pop_moe_num_experts(None) == -1
+    lib.pop_moe_destroy(None)  # no-op

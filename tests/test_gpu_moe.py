@@ -1,0 +1,266 @@
+"""MoE layer of POP-pruned experts on the GPU against the oracle (top-2 routing, per-expert
+partition from the routed prompt tokens, per-expert decode on routed tokens, weighted combine).
+
+Tiny layers are checked in full; the 8-expert D=4096, D_FF=14336 layer with a 4096-token prompt and
+B=32 decode steps is checked on its routing (every token, exact), the counting rule on each
+expert's own importance, sampled channels and rows of the prefill, and full decode steps on
+partitions the oracle computes from a short prompt.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import parity
+
+pytestmark = pytest.mark.gpu
+
+f64 = synth.bf16_to_f64
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import online_structured_ffn_gb300 as pop
+    torch.cuda.set_device(0)
+    return pop, torch, torch.device("cuda", 0)
+
+
+def up(env, a):
+    _, torch, dev = env
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def logits_t(env, L):
+    _, torch, dev = env
+    return torch.from_numpy(np.ascontiguousarray(L, dtype=np.float32)).to(dev)
+
+
+class Moe:
+    def __init__(self, env, E, D, N, seed=0, **kw):
+        pop = env[0]
+        self.E, self.D, self.N, self.seed = E, D, N, seed
+        self.w = [synth.ffn_weights(seed, D, N, layer=e) for e in range(E)]
+        self.sc = synth.dim_scales(seed, D)
+        self.moe = pop.PopMoE([up(env, w[0]) for w in self.w], [up(env, w[1]) for w in self.w],
+                              [up(env, w[2]) for w in self.w], **kw)
+        self.counts = self.moe.counts
+
+    def w64(self, e):
+        return tuple(f64(a) for a in self.w[e])
+
+    def close(self):
+        self.moe.close()
+
+
+def _check_prefill_y(Y, Y_ref, X, L, w64, rows=None, what="MoE prefill Y", bf16_out=False):
+    """Prefill Y is made from bf16-rounded Z (the down GEMM's operand): rel-L2 <= 5e-3 and, per
+    element, |Y - Y_ref| <= sum over the token's experts of w * 2^-8 (|Z| |W2|^T), the bf16
+    rounding bound of a single layer's prefill weighted like the outputs (plus 2^-8 |Y| when the
+    output itself is rounded to bf16)."""
+    ex, w = oracle.moe_route(np.asarray(L, dtype=np.float32))
+    rows = np.arange(X.shape[0]) if rows is None else np.asarray(rows)
+    bound = np.zeros((len(rows), X.shape[1]))
+    for e in sorted(set(ex[rows].ravel().tolist())):
+        Wg, W1, W2 = w64(e)
+        for i, t in enumerate(rows):
+            for j in range(2):
+                if ex[t, j] == e:
+                    Z = oracle.ffn_activations(Wg, W1, f64(X[t:t + 1]))
+                    bound[i] += w[t, j] * 2.0 ** -8 * (np.abs(Z) @ np.abs(W2).T)[0]
+    if bf16_out:
+        bound += 2.0 ** -8 * np.abs(Y_ref)
+    assert parity.rel_l2(Y, Y_ref) <= parity.Y_REL_L2, what
+    assert np.all(np.abs(Y - Y_ref) <= bound + 1e-6), f"{what}: max excess {np.max(np.abs(Y - Y_ref) - bound):.3e}"
+
+
+def _check_routing(moe, L):
+    ex_ref, w_ref = oracle.moe_route(np.asarray(L, dtype=np.float32))
+    ex, w = moe.routing()
+    assert np.array_equal(ex, ex_ref)
+    np.testing.assert_allclose(w, w_ref, rtol=2e-6, atol=1e-7)
+    return ex_ref
+
+
+def _decode_steps(env, m, parts, B, steps, check_sel=True):
+    """Decode on the given partitions; compares routing, selections and outputs every step."""
+    _, torch, dev = env
+    for e in range(m.E):
+        m.moe.experts[e].set_partition(parts[e]["R"], parts[e]["C"], parts[e]["P"])
+    xs = [synth.decode_input(m.seed, t, B, m.sc) for t in range(steps)]
+    Ls = [synth.router_logits(m.seed, B, m.E, step=t).astype(np.float32) for t in range(steps)]
+    ys_ref, per = oracle.moe_decode(m.w64, parts, [f64(x) for x in xs], Ls, m.counts.k)
+    # the GPU runs step by step; the selections are read after each step
+    flips = 0
+    for t in range(steps):
+        y = m.moe.decode_step(up(env, xs[t]), logits_t(env, Ls[t])).float().cpu().numpy()
+        ex = _check_routing(m.moe, Ls[t])
+        assert np.array_equal(m.moe.token_counts(), np.bincount(ex.ravel(), minlength=m.E))
+        flipped = set()
+        for e in range(m.E):
+            if check_sel and m.counts.k:
+                r = per[e][t]
+                bad, _, nd = parity.compare_selection(m.moe.experts[e].selected(), r["S"], r["C"], r["scores"],
+                                                      m.counts.k)
+                assert not bad, f"step {t} expert {e}: selection differs outside the flagged band: {bad[:8]}"
+                if nd:
+                    flipped.add(e)
+        flips += len(flipped)
+        rows = [b for b in range(B) if not (set(ex[b].tolist()) & flipped)]
+        parity.check_y(y[rows], ys_ref[t][rows], f"B={B} step {t}")
+    for e in range(m.E):
+        assert m.moe.experts[e].step_count() == steps
+    m.moe.check()
+    return flips
+
+
+@pytest.mark.parametrize("B", [1, 5, 16, 32])
+def test_moe_prefill_and_decode(env, B):
+    _, torch, dev = env
+    E, D, N, M, r, gamma = 4, 256, 1024, 64, 0.3, 0.1
+    m = Moe(env, E, D, N, r=r, gamma=gamma, max_batch=B, max_prefill_tokens=32)
+    X = synth.prompt(m.seed, M, m.sc)
+    L = synth.router_logits(m.seed, M, E).astype(np.float32)
+    Y = torch.empty((M, D), dtype=torch.float32, device=dev)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
+    m.moe.check()
+    ex = _check_routing(m.moe, L)
+    assert np.array_equal(m.moe.token_counts(), np.bincount(ex.ravel(), minlength=E))
+    ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, r, gamma)
+    for e in range(E):
+        p = ref["parts"][e]
+        bad, _, _ = parity.compare_partition(m.moe.experts[e].partition(), (p["R"], p["C"], p["P"]), p["I"],
+                                             p["counts"])
+        assert len(bad) == 0, f"expert {e}: partition differs outside the flagged band: {bad[:10]}"
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64)
+    _decode_steps(env, m, ref["parts"], B, steps=4)
+    m.close()
+
+
+def test_moe_idle_experts(env):
+    """Experts that get no prompt token split by the index tie rule; in decode they select the
+    lowest candidate positions and contribute nothing."""
+    _, torch, dev = env
+    E, D, N, M, B = 4, 256, 512, 32, 6
+    m = Moe(env, E, D, N, seed=3, r=0.3, gamma=0.1, max_batch=B, max_prefill_tokens=64)
+    X = synth.prompt(m.seed, M, m.sc)
+    L = np.full((M, E), -4.0, dtype=np.float32)
+    L[:, 0], L[:, 1] = 1.0, 0.25
+    Y = torch.empty((M, D), dtype=torch.float32, device=dev)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
+    m.moe.check()
+    assert m.moe.token_counts().tolist() == [M, M, 0, 0]
+    c = m.counts
+    for e in (2, 3):
+        R, C, P = m.moe.experts[e].partition()
+        assert R.tolist() == list(range(c.n_R))
+        assert C.tolist() == list(range(c.n_R, N - c.n_P))
+        assert P.tolist() == list(range(N - c.n_P, N))
+    ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, 0.3, 0.1)
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64, what="MoE prefill Y with idle experts")
+    x = synth.decode_input(m.seed, 0, B, m.sc)
+    Lt = np.full((B, E), -4.0, dtype=np.float32)
+    Lt[:, 1], Lt[:, 0] = 2.0, 1.0
+    y = m.moe.decode_step(up(env, x), logits_t(env, Lt)).cpu().numpy()
+    m.moe.check()
+    for e in (2, 3):
+        assert m.moe.experts[e].selected().tolist() == list(range(c.n_R, c.n_R + c.k))
+        assert m.moe.experts[e].step_count() == 1
+    ys_ref, _ = oracle.moe_decode(m.w64, ref["parts"], [f64(x)], [Lt], c.k)
+    parity.check_y(y, ys_ref[0], "MoE decode y with idle experts")
+    m.close()
+
+
+def test_moe_bf16_output_and_errors(env):
+    pop, torch, dev = env
+    E, D, N, M, B = 3, 264, 1000, 40, 4
+    m = Moe(env, E, D, N, seed=5, r=0.299, gamma=0.1, max_batch=B, max_prefill_tokens=16, out_f32=False)
+    x = synth.decode_input(m.seed, 0, B, m.sc)
+    Lx = synth.router_logits(m.seed, B, E, step=0).astype(np.float32)
+    with pytest.raises(pop.PopError) as err:  # decode before any partition
+        m.moe.decode_step(up(env, x), logits_t(env, Lx))
+    assert err.value.status == pop.POP_ERR_STATE
+    X = synth.prompt(m.seed, M, m.sc)
+    L = synth.router_logits(m.seed, M, E).astype(np.float32)
+    Y = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
+    ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, 0.299, 0.1)
+    _check_prefill_y(Y.float().cpu().numpy(), ref["Y"], X, L, m.w64, what="MoE prefill Y (bf16 out)",
+                     bf16_out=True)
+    with pytest.raises(pop.PopError) as err:
+        m.moe.decode_step(up(env, np.concatenate([x, x])), logits_t(env, np.concatenate([Lx, Lx])))
+    assert err.value.status == pop.POP_ERR_INVALID_ARG  # B > max_batch
+    y = m.moe.decode_step(up(env, x), logits_t(env, Lx))
+    assert y.dtype == torch.bfloat16
+    ys_ref, _ = oracle.moe_decode(m.w64, ref["parts"], [f64(x)], [Lx], m.counts.k)
+    # the GPU decodes on its own prefill partition here; compare where every expert's set agrees
+    same = all(np.array_equal(m.moe.experts[e].partition()[0], ref["parts"][e]["R"]) and
+               np.array_equal(m.moe.experts[e].partition()[1], ref["parts"][e]["C"]) for e in range(E))
+    if same:
+        parity.check_y(y.float().cpu().numpy(), ys_ref[0], "MoE decode y (bf16 out)")
+    m.moe.check()
+    m.close()
+
+
+def test_moe_full_size(env):
+    """8 experts, D=4096, D_FF=14336, r=0.3, top-2 of a 4096-token prompt, B=32 decode."""
+    _, torch, dev = env
+    E, D, N, M, B, r, gamma = 8, 4096, 14336, 4096, 32, 0.3, 0.1
+    m = Moe(env, E, D, N, r=r, gamma=gamma, max_batch=B, max_prefill_tokens=2048)
+    X = synth.prompt(m.seed, M, m.sc)
+    L = synth.router_logits(m.seed, M, E).astype(np.float32)
+    Y = torch.empty((M, D), dtype=torch.float32, device=dev)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
+    m.moe.check()
+    ex = _check_routing(m.moe, L)
+    counts = np.bincount(ex.ravel(), minlength=E)
+    assert np.array_equal(m.moe.token_counts(), counts) and counts.sum() == 2 * M
+    _, w_ref = oracle.moe_route(L)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(M, 3, replace=False))
+    Yg = Y.cpu().numpy()[rows]
+    Yr = np.zeros((len(rows), D))
+    bound = np.zeros((len(rows), D))
+    Xf = f64(X)
+    for e in range(E):
+        R, C, P = m.moe.experts[e].partition()
+        I, ss = m.moe.experts[e].importance()
+        R0, C0, P0 = oracle.partition(I, oracle.region_counts(N, r, gamma))
+        assert np.array_equal(R, R0) and np.array_equal(C, C0) and np.array_equal(P, P0), f"expert {e}"
+        tok = np.nonzero(np.any(ex == e, axis=1))[0]
+        Wg, W1, W2 = m.w64(e)
+        if e < 2:  # sampled channels' sum of z^2 over the routed tokens
+            ch = np.sort(rng.choice(N, 48, replace=False))
+            Z = oracle.ffn_activations(Wg[ch], W1[ch], Xf[tok])
+            ss_ref, _ = oracle.channel_importance(W2[:, ch], Z)
+            assert np.all(np.abs(ss[ch] - ss_ref) <= 1e-4 * ss_ref + 1e-7 * ss_ref.max()), f"expert {e}"
+        for i, t in enumerate(rows):
+            for j in range(2):
+                if ex[t, j] == e:
+                    Z = oracle.ffn_activations(Wg, W1, Xf[t:t + 1])
+                    Yr[i] += w_ref[t, j] * oracle.down_projection(W2, Z)[0]
+                    bound[i] += w_ref[t, j] * 2.0 ** -8 * (np.abs(Z) @ np.abs(W2).T)[0]
+        del Wg, W1, W2
+    # prefill Y comes from bf16-rounded Z: the single-layer prefill bound, weighted like the outputs
+    assert parity.rel_l2(Yg, Yr) <= parity.Y_REL_L2
+    assert np.all(np.abs(Yg - Yr) <= bound + 1e-6), f"max excess {np.max(np.abs(Yg - Yr) - bound):.3e}"
+    # decode on partitions the oracle takes from a short prompt (8 tokens, top-2: some experts idle)
+    Xs = synth.prompt(m.seed, 8, m.sc)
+    Ls = L[:8]
+    ex_s, _ = oracle.moe_route(Ls)
+    parts = []
+    for e in range(E):
+        tok = np.nonzero(np.any(ex_s == e, axis=1))[0]
+        Wg, W1, W2 = m.w64(e)
+        if tok.size:
+            pre = oracle.prefill(Wg, W1, W2, f64(Xs)[tok], r, gamma)
+            parts.append(dict(R=pre["R"], C=pre["C"], P=pre["P"]))
+        else:
+            R, C, P = oracle.partition(np.zeros(N), oracle.region_counts(N, r, gamma))
+            parts.append(dict(R=R, C=C, P=P))
+        del Wg, W1, W2
+    _decode_steps(env, m, parts, B, steps=2)
+    m.close()

@@ -476,3 +476,20 @@ def test_moe_token_permutation_permutes_outputs():
     Lt = np.random.default_rng(6).normal(size=(6, E))
     q = np.random.default_rng(7).permutation(6)
     np.testing.assert_allclose(sb.step(x[q], Lt[q]), sa.step(x, Lt)[q], rtol=1e-12, atol=1e-14)
+
+
+def test_moe_decode_expert_major_equals_stepping_the_layer():
+    D, N, E = 16, 48, 4
+    ex = _moe_experts(E, D, N)
+    pre = oracle.moe_prefill(ex, _x(45, 12, D), np.random.default_rng(8).normal(size=(12, E)), 0.3, 0.1)
+    k = pre["parts"][0]["counts"].k
+    xs = [_x(45, 5, D, step=t) for t in range(4)]
+    Ls = [np.random.default_rng(30 + t).normal(size=(5, E)) for t in range(4)]
+    ys, per = oracle.moe_decode(lambda e: ex[e], pre["parts"], xs, Ls, k, period=2)
+    sess = oracle.MoeSession([oracle.PopSession(*ex[e], pre["parts"][e]["R"], pre["parts"][e]["C"], k, period=2)
+                              for e in range(E)])
+    for t in range(4):
+        np.testing.assert_array_equal(ys[t], sess.step(xs[t], Ls[t]))
+        for e in range(E):
+            s = sess.sessions[e]
+            assert per[e][t]["S"].tolist() == s.C[s.S].tolist()
