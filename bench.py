@@ -585,11 +585,14 @@ def main():
     if args.decode_steps > 0:
         WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], T=args.decode_steps)
     wl = WORKLOADS[args.workload]
-    config = {"workload": args.workload, "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
+    moe_keys = {"experts": wl["experts"], "routing": "top-2"} if wl.get("experts") else {}
+    config = {"workload": args.workload, **moe_keys, "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
               "B": wl["B"], "prompt_tokens": wl["M"], "decode_steps": wl["T"], "period": wl["period"],
               "layers": wl["layers"],
-              "l2": "inputs larger than L2: each decode step reads another layer's weights "
-                    f"({wl['layers']} layers x {3 * wl['D'] * wl['N'] * 2 / 1e6:.0f} MB)",
+              "l2": ("inputs larger than L2: each decode step streams every expert's weights "
+                     f"({wl['experts']} experts x {3 * wl['D'] * wl['N'] * 2 / 1e6:.0f} MB)" if wl.get("experts") else
+                     "inputs larger than L2: each decode step reads another layer's weights "
+                     f"({wl['layers']} layers x {3 * wl['D'] * wl['N'] * 2 / 1e6:.0f} MB)"),
               "parallelism": "replicas" if world > 1 else "single-gpu"}
 
     if args.impl == "reference":
