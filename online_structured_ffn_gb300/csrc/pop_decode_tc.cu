@@ -42,8 +42,10 @@
 // decode, gathered columns in the dense reference path), then gathers its share of the selected
 // items.
 // The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
-// writes the selected channels and their z planes, and releases a flag; the other CTAs wait
-// (bounded) for the flag only when they reach their first selected item. The partial accumulators
+// writes the selected positions and channels, and releases a flag. The other CTAs wait (bounded)
+// for the flag when they reach their first selected item; then each producer warp packs a share of
+// the selected items' z planes (a few items each, so no one CTA moves them all) and waits (bounded)
+// until every share is done. The partial accumulators
 // of a split unit are added through distributed shared memory in rank order (a fixed order:
 // results do not depend on timing). No workspace, no atomics on data.
 //
@@ -101,7 +103,9 @@ struct TcCtl {
   uint32_t tmem_base;
   int abort_flag;
   int seg_ok[2];  // by unit parity: a warp may still read one while the next is written
-  unsigned sel_seen;  // down: the selection epoch warp 0 has seen complete
+  unsigned pack_seen;  // down: the epoch whose selected z planes every packer has written
+  int epi_ok;          // down: the selection wait of the epilogue warps succeeded
+  int pack_pos[128];   // down: positions of a chunk of selected items being packed
 };
 
 template <int NP>
@@ -186,14 +190,14 @@ struct ProdSync {
 
 // ------------------------------------------------------------------ selection (down, first cluster)
 // Updates the periodic memory and selects the k best candidates when the step is an update step
-// (select_step, warps 0-7), then, with all 416 threads, writes the selected candidates' channels and
-// the hi / lo bf16 parts of their z at columns 64 * kbr + j of the z planes, advances the step
-// counter and releases the flag. S is kept in shared memory next to the keys when both fit.
+// (select_step, warps 0-7), writes the selected positions (update steps) and their channels,
+// advances the step counter, clears the other step parity's pack counter and releases the flag.
+// The z planes of the selected items are then packed by the GEMM CTAs, each a share (one CTA
+// alone moves them at a fraction of the bandwidth while the others stream).
 __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_PROD_THREADS>& rsc) {
   // While the GEMM CTAs stream, every global access of this CTA waits behind their requests
   // (microseconds), so all inputs are fetched in one round at the start, into shared memory:
-  //   [keys: nC u32 | scores: nC f32 | channels of C: nC i32 | S: k i32 | z of C: nC x ldzc f32]
-  // (z only when it fits; otherwise the pack reads it from global memory).
+  //   [keys: nC u32 | scores: nC f32 | channels of C: nC i32 | S: k i32 | memory: nC f32 (period > 1)]
   const int tid = threadIdx.x;
   const int nC = a.nC, k = a.k;
   uint32_t dyn = 0;
@@ -201,32 +205,28 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
   const size_t avail = dyn > 1024 ? dyn - 1024 : 0;
   auto al16 = [](size_t v) { return (v + 15) & ~size_t(15); };
   const size_t o_keys = 0, o_sc = al16(static_cast<size_t>(nC) * 4), o_rc = o_sc + al16(static_cast<size_t>(nC) * 4);
-  const size_t o_S = o_rc + al16(static_cast<size_t>(nC) * 4), o_z = o_S + al16(static_cast<size_t>(k) * 4);
-  const bool small = o_z <= avail;  // scores, channels and S in shared memory
-  const bool zin = small && o_z + static_cast<size_t>(nC) * a.ldzc * 4 <= avail;
+  const size_t o_S = o_rc + al16(static_cast<size_t>(nC) * 4), o_m = o_S + al16(static_cast<size_t>(k) * 4);
+  const bool periodic = a.period > 1;
+  const bool small = o_m + (periodic ? al16(static_cast<size_t>(nC) * 4) : 0) <= avail;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + o_keys);
   float* s_sc = reinterpret_cast<float*>(smem + o_sc);
   int* s_rc = reinterpret_cast<int*>(smem + o_rc);
   int* sS = small ? reinterpret_cast<int*>(smem + o_S) : a.S;
-  float* s_z = reinterpret_cast<float*>(smem + o_z);
+  float* mem = small && periodic ? reinterpret_cast<float*>(smem + o_m) : a.memory;
   const int t = *a.step;
   const bool update = (t % a.period) == 0;
   if (small) {
     const uint32_t sb = smem_u32(smem);
     for (int i = tid; i < (nC + 3) / 4; i += TC_THREADS) {
-      const int n = min(4, nC - 4 * i);
-      cp_async16(sb + static_cast<uint32_t>(o_sc) + 16u * i, a.scores + 4 * i, 4u * n);
-      cp_async16(sb + static_cast<uint32_t>(o_rc) + 16u * i, a.rc + 4 * i, 4u * n);
+      const uint32_t n = 4u * static_cast<uint32_t>(min(4, nC - 4 * i));
+      cp_async16(sb + static_cast<uint32_t>(o_sc) + 16u * i, a.scores + 4 * i, n);
+      cp_async16(sb + static_cast<uint32_t>(o_rc) + 16u * i, a.rc + 4 * i, n);
+      if (periodic) cp_async16(sb + static_cast<uint32_t>(o_m) + 16u * i, a.memory + 4 * i, n);
     }
     if (!update)  // the held selection of the last update step
       for (int i = tid; i < (k + 3) / 4; i += TC_THREADS)
         cp_async16(sb + static_cast<uint32_t>(o_S) + 16u * i, a.S + 4 * i, 4u * min(4, k - 4 * i));
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    if (zin) {  // z lands while the top-k runs
-      const int nz = nC * (a.ldzc / 4);  // ldzc is a multiple of 4: whole 16-byte chunks
-      for (int i = tid; i < nz; i += TC_THREADS) cp_async16(sb + static_cast<uint32_t>(o_z) + 16u * i, a.zc + 4 * i, 16u);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 1;" ::: "memory");
+    cp_async_wait_all();
   }
   __syncthreads();
   __shared__ int s_sel;
@@ -234,12 +234,13 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
     bool sel = true;
     if (nC > 0)
       sel = select_step<TC_PROD_THREADS>(
-          tid, [&](int i) { return small ? s_sc[i] : __ldcg(a.scores + i); }, a.memory, nC, k, a.period, update, keys,
+          tid, [&](int i) { return small ? s_sc[i] : __ldcg(a.scores + i); }, mem, nC, k, a.period, update, keys,
           sS, rsc, ProdSync());
     if (tid == 0) s_sel = sel ? 1 : 0;
   }
-  if (small) cp_async_wait_all();  // z of the candidates
   __syncthreads();
+  if (small && periodic)  // the memory as select_step left it (summed, or cleared on an update)
+    for (int i = tid; i < nC; i += TC_THREADS) a.memory[i] = mem[i];
   if (update && small)
     for (int j = tid; j < k; j += TC_THREADS) a.S[j] = sS[j];
   // channels of the selected candidates
@@ -249,50 +250,15 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
       atomicOr(a.err, DEVERR_INDEX);
       ps = 0;
       sS[j] = 0;
+      if (update && small) a.S[j] = 0;
     }
     a.ch_s[j] = guard_ch(small ? s_rc[ps] : __ldg(a.rc + ps), a.N, a.err);
-  }
-  __syncthreads();
-  // z planes of the selected items: task (8 items from j0 = 8 o, 4 tokens from 4 q): eight float4
-  // reads of z, then per token one 16-byte store of eight hi parts and one of eight lo parts
-  uint16_t* zk = const_cast<uint16_t*>(a.zk);
-  uint16_t* zk_lo = zk + a.zk_lo_off;
-  const int col0 = 64 * a.kbr;
-  const int nq = a.ldzc >> 2, no = (k + 7) >> 3;
-  const int tasks = no * nq;
-  for (int e = tid; e < tasks; e += TC_THREADS) {
-    const int o = e % no, q = e / no;
-    float4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = 8 * o + i;
-      const size_t zo = j < k ? static_cast<size_t>(sS[j]) * a.ldzc + 4 * q : 0;
-      v[i] = j >= k ? make_float4(0.f, 0.f, 0.f, 0.f)
-                    : (zin ? *reinterpret_cast<const float4*>(s_z + zo) : __ldcg(reinterpret_cast<const float4*>(a.zc + zo)));
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int b = 4 * q + c;
-      if (b >= a.B) break;
-      uint16_t hi[8], lo[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float f = c == 0 ? v[i].x : (c == 1 ? v[i].y : (c == 2 ? v[i].z : v[i].w));
-        split_bf16(f, hi[i], lo[i]);
-      }
-      const size_t off = static_cast<size_t>(b) * a.ldk + col0 + 8 * o;
-      *reinterpret_cast<uint4*>(zk + off) =
-          make_uint4(hi[0] | (uint32_t(hi[1]) << 16), hi[2] | (uint32_t(hi[3]) << 16), hi[4] | (uint32_t(hi[5]) << 16),
-                     hi[6] | (uint32_t(hi[7]) << 16));
-      *reinterpret_cast<uint4*>(zk_lo + off) =
-          make_uint4(lo[0] | (uint32_t(lo[1]) << 16), lo[2] | (uint32_t(lo[3]) << 16), lo[4] | (uint32_t(lo[5]) << 16),
-                     lo[6] | (uint32_t(lo[7]) << 16));
-    }
   }
   __syncthreads();
   if (tid == 0) {
     if (!s_sel) atomicOr(a.err, DEVERR_TOPK);
     if (a.count_step) *a.step = t + 1;
+    a.pack_cnt[(a.epoch + 1u) & 1u] = 0u;  // the next step's counter; this step's was cleared by the last
     __threadfence();
     st_release_u32(a.flag, a.epoch);
   }
@@ -1002,7 +968,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   }
 
   volatile int* abort_flag = &ctl.abort_flag;
-  volatile unsigned* sel_seen = &ctl.sel_seen;
+  volatile unsigned* pack_seen = &ctl.pack_seen;
   const int unit0 = ci - a.sel, nunits = static_cast<int>(gridDim.x) / SK - a.sel;
   const int U = a.units;
   const int G = a.D / 8;  // output groups of 8 (16 bytes); a unit is a range of whole groups
@@ -1016,6 +982,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   const int r0 = static_cast<int>(rank) * a.kbr / SK, r1 = (static_cast<int>(rank) + 1) * a.kbr / SK;
   const int s0 = static_cast<int>(rank) * kbs / SK, s1 = (static_cast<int>(rank) + 1) * kbs / SK;
   const int nblk = (r1 - r0) + (s1 - s0);  // stages per unit
+  // Packers of the selected items' z planes: every CTA that has units and selected blocks (npk of
+  // them); its epilogue warps pack a share as soon as the selection is out, while its producers
+  // still stream R.
+  int rws = 0, rbefore = 0;  // ranks with selected blocks; those of them before this rank
+  for (int r = 0; r < SK; ++r) {
+    const int hs = (r + 1) * kbs / SK > r * kbs / SK ? 1 : 0;
+    rws += hs;
+    if (r < static_cast<int>(rank)) rbefore += hs;
+  }
+  const int npk = min(nunits, U) * rws;
+  const int pid = unit0 * rws + rbefore;
+  const bool packer = a.sel && a.k > 0 && unit0 < U && s1 > s0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1029,7 +1007,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     }
     mbar_init(&ctl.drain, 1);
     ctl.abort_flag = 0;
-    ctl.sel_seen = a.epoch - 1u;
+    ctl.pack_seen = a.epoch - 1u;
     fence_mbar_init();
   }
   if (warp == TC_MMA_WARP) {
@@ -1131,35 +1109,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
       const bool dok = d0 < hi;
       for (int bi = 0; bi < nblk; ++bi) {
         if (bi == nrs && bi < nblk) {
-          // first selected block: the selection of this step must be complete. Warp 0 polls the
-          // flag in global memory and posts what it saw in shared memory; the other warps watch
-          // that (every wait bounded; no barrier across warps that a warp which gave up earlier
-          // would miss).
+          // first selected block: the selected items' z planes of this step must be complete (the
+          // epilogue warps post it in shared memory once every packer has counted; every wait bounded)
           int good = 1;
           if (lane == 0) {
             const uint64_t t0 = globaltimer_ns();
-            if (warp == 0) {
-              while (static_cast<int>(ld_acquire_u32(a.flag) - a.epoch) < 0) {
-                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
-                  good = 0;
-                  break;
-                }
-                __nanosleep(256);
+            while (static_cast<int>(*pack_seen - a.epoch) < 0) {
+              if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+                good = 0;
+                break;
               }
-              if (good) {
-                __threadfence_block();
-                *sel_seen = a.epoch;
-              }
-            } else {
-              while (static_cast<int>(*sel_seen - a.epoch) < 0) {
-                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
-                  good = 0;
-                  break;
-                }
-                __nanosleep(64);
-              }
-              if (good) (void)ld_acquire_u32(a.flag);  // acquire for this warp's own reads
+              __nanosleep(64);
             }
+            if (good) (void)ld_acquire_u32(a.pack_cnt + (a.epoch & 1u));  // acquire for this warp's reads
             if (!good) fail();
           }
           good = __shfl_sync(0xffffffffu, good, 0);
@@ -1278,6 +1240,88 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const int et = threadIdx.x - 32 * TC_EPI0;
+    if (packer) {
+      // This CTA's share of the selected items, j in [j0, j1): once the selection is out, z of each
+      // (fp32, from the gate/up) split into hi / lo bf16 parts at column 64 kbr + j of the z planes,
+      // then one release count per CTA and a bounded wait until all npk packers have counted.
+      if (et == 0) {
+        int good = 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (static_cast<int>(ld_acquire_u32(a.flag) - a.epoch) < 0) {
+          if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+            good = 0;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (!good) fail();
+        ctl.epi_ok = good;
+      }
+      epi_bar();
+      const bool go = ctl.epi_ok != 0;
+      if (go && lane == 0) (void)ld_acquire_u32(a.flag);  // acquire for this warp's own reads
+      __syncwarp();
+      const unsigned up = static_cast<unsigned>(pid), un = static_cast<unsigned>(npk);
+      const int j0 = static_cast<int>(up * static_cast<unsigned>(a.k) / un);
+      const int j1 = static_cast<int>((up + 1u) * static_cast<unsigned>(a.k) / un);
+      uint16_t* zk = const_cast<uint16_t*>(a.zk);
+      const int col0 = TC_BK * a.kbr;
+      for (int c = j0; go && c < j1; c += 128) {
+        const int ncj = min(128, j1 - c);
+        if (et < ncj) {
+          int ps = __ldcg(a.S + c + et);
+          if (static_cast<unsigned>(ps) >= static_cast<unsigned>(a.nC)) {
+            atomicOr(a.err, DEVERR_INDEX);
+            ps = 0;
+          }
+          ctl.pack_pos[et] = ps;
+        }
+        epi_bar();
+        const int total = ncj * a.B;
+        for (int e0 = 0; e0 < total; e0 += 128 * 8) {
+          float zv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e = e0 + 128 * u + et;
+            zv[u] = e < total ? __ldcg(a.zc + static_cast<size_t>(ctl.pack_pos[e % ncj]) * a.ldzc + e / ncj) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int e = e0 + 128 * u + et;
+            if (e < total) {
+              uint16_t h16, l16;
+              split_bf16(zv[u], h16, l16);
+              const size_t o = static_cast<size_t>(e / ncj) * a.ldk + col0 + c + e % ncj;
+              zk[o] = h16;
+              zk[a.zk_lo_off + o] = l16;
+            }
+          }
+        }
+        epi_bar();  // pack_pos is reused by the next chunk
+      }
+      __threadfence();
+      epi_bar();
+      if (et == 0 && go) {
+        unsigned* cnt = a.pack_cnt + (a.epoch & 1u);
+        __threadfence();  // with the barrier: every epilogue thread's planes before the count
+        atomicAdd(cnt, 1u);
+        int good = 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u32(cnt) < un) {
+          if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+            good = 0;
+            break;
+          }
+          __nanosleep(128);
+        }
+        if (good) {
+          __threadfence_block();
+          *pack_seen = a.epoch;
+        } else {
+          fail();
+        }
+      }
+    }
     int it = 0;
     for (int unit = unit0; unit < U; unit += nunits, ++it) {
       const int buf = it & 1;
@@ -1466,11 +1510,12 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   constexpr size_t kMaxDyn = 227 * 1024 - kStatic;
   const size_t c16 = (static_cast<size_t>(a.nC) * 4 + 15) & ~size_t(15);
   const size_t keys_bytes = 1024 + c16;
-  const size_t small_bytes = keys_bytes + 2 * c16 + ((static_cast<size_t>(a.k) * 4 + 15) & ~size_t(15));
-  const size_t z_bytes = small_bytes + static_cast<size_t>(a.nC) * a.ldzc * 4;
+  // the selecting CTA: keys, scores, channels of C, S and (periodic) the memory in shared memory
+  const size_t small_bytes = keys_bytes + 2 * c16 + ((static_cast<size_t>(a.k) * 4 + 15) & ~size_t(15)) +
+                             (a.period > 1 ? c16 : 0);
   if (a.sel) {
     if (keys_bytes > kMaxDyn) return cudaErrorInvalidValue;  // |C| beyond what one CTA's keys can hold
-    const size_t want = z_bytes <= kMaxDyn ? z_bytes : (small_bytes <= kMaxDyn ? small_bytes : keys_bytes);
+    const size_t want = small_bytes <= kMaxDyn ? small_bytes : keys_bytes;
     if (want > smem) smem = want;
   }
   static size_t configured = 0;

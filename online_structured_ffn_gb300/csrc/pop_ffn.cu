@@ -64,7 +64,8 @@ struct pop_ffn {
 };
 
 static constexpr int kProfEvents = 5;
-// device counters: [4] candidates scored by the B = 1 gate/up, [8..] tiles of y done by the down chunks
+// device counters: [4] candidates scored by the B = 1 gate/up, [5] the B > 1 selection flag, [6, 7]
+// the B > 1 pack counters, [8..] tiles of y done by the B = 1 down chunks
 static constexpr int kSyncWords = 64;
 static constexpr int kProfMaxSteps = 256;
 
@@ -262,6 +263,7 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.count_step = decode ? 1 : 0;
   a.flag = h->fsync + 5;
   a.epoch = decode ? ++h->epoch : 0;
+  a.pack_cnt = h->fsync + 6;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   POP_CUDA(h, launch_down_tc(a, h->num_sms, st));

@@ -76,6 +76,8 @@ struct DownTcArgs {
   int count_step;        // 1: advance the step counter (decode)
   unsigned* flag;        // selection of step `epoch` complete when *flag == epoch
   unsigned epoch;
+  unsigned* pack_cnt;    // [2], by epoch parity: producer warps that have packed their share of the
+                         // selected items' z planes this step (the selecting CTA clears the other one)
   // work split (set by the launcher)
   int split, units;
   unsigned* err;
