@@ -43,9 +43,9 @@
 // items.
 // The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
 // writes the selected positions and channels, and releases a flag. The other CTAs wait (bounded)
-// for the flag when they reach their first selected item; then each producer warp packs a share of
-// the selected items' z planes (a few items each, so no one CTA moves them all) and waits (bounded)
-// until every share is done. The partial accumulators
+// for the flag when they reach their first selected item. A selected item's z comes as the MMA's
+// MN-major B operand: the gate/up writes each candidate's z as one row of 2 NP bf16 (hi parts of
+// the tokens, then lo parts), which the producers gather like the down columns. The partial accumulators
 // of a split unit are added through distributed shared memory in rank order (a fixed order:
 // results do not depend on timing). No workspace, no atomics on data.
 //
@@ -81,12 +81,16 @@ constexpr int DN_WIN_WORDS = 8 * DN_WIN * 8;
 constexpr int DN_PRE = 2;  // stages of down columns issued before waiting for the previous kernel
 constexpr int GU_PRE = 2;         // stages of weights issued before waiting for the previous kernel
 
-// Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major), B = the hi
-// and lo planes of z, NP rows each.
+// Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major). B = z of the
+// 64 items for 2 NP columns (the hi and lo parts of NP tokens): for R items K-major (the z planes,
+// one 128-byte row per column), for selected items MN-major (one 128-byte row per item holding up
+// to 64 columns, atoms of 64 columns 8 KB apart), gathered from the gate/up's candidate rows.
 template <int NP>
 struct DnCfg {
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
-  static constexpr uint32_t B_BYTES = 2 * NP * TC_BK * 2;
+  static constexpr uint32_t B_KMAJOR = 2 * NP * TC_BK * 2;
+  static constexpr uint32_t B_MNMAJOR = TC_BK * 128 * ((2 * NP + 63) / 64);
+  static constexpr uint32_t B_BYTES = B_KMAJOR > B_MNMAJOR ? B_KMAJOR : B_MNMAJOR;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = TC_RING / STAGE_BYTES < 12 ? TC_RING / STAGE_BYTES : 12;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
@@ -103,9 +107,7 @@ struct TcCtl {
   uint32_t tmem_base;
   int abort_flag;
   int seg_ok[2];  // by unit parity: a warp may still read one while the next is written
-  unsigned pack_seen;  // down: the epoch whose selected z planes every packer has written
-  int epi_ok;          // down: the selection wait of the epilogue warps succeeded
-  int pack_pos[128];   // down: positions of a chunk of selected items being packed
+  unsigned sel_seen;  // down: the selection epoch warp 0 has seen complete
 };
 
 template <int NP>
@@ -128,6 +130,25 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
   const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
   hi = *reinterpret_cast<const uint16_t*>(&h);
   lo = *reinterpret_cast<const uint16_t*>(&l);
+}
+
+// n (a multiple of 8) values as bf16 hi parts at hi[0..n) and lo parts at lo[0..n): 16-byte stores
+template <int n>
+__device__ __forceinline__ void store_hilo(uint16_t* hi, uint16_t* lo, const float* v) {
+#pragma unroll
+  for (int c = 0; c < n; c += 8) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint16_t h0, l0, h1, l1;
+      split_bf16(v[c + 2 * i], h0, l0);
+      split_bf16(v[c + 2 * i + 1], h1, l1);
+      h[i] = h0 | (static_cast<uint32_t>(h1) << 16);
+      l[i] = l0 | (static_cast<uint32_t>(l1) << 16);
+    }
+    *reinterpret_cast<uint4*>(hi + c) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + c) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros (nothing is read). No
@@ -191,9 +212,8 @@ struct ProdSync {
 // ------------------------------------------------------------------ selection (down, first cluster)
 // Updates the periodic memory and selects the k best candidates when the step is an update step
 // (select_step, warps 0-7), writes the selected positions (update steps) and their channels,
-// advances the step counter, clears the other step parity's pack counter and releases the flag.
-// The z planes of the selected items are then packed by the GEMM CTAs, each a share (one CTA
-// alone moves them at a fraction of the bandwidth while the others stream).
+// advances the step counter and releases the flag. The GEMM CTAs then gather the selected items'
+// z straight from the gate/up's candidate rows (an MN-major operand), so nothing is packed here.
 __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_PROD_THREADS>& rsc) {
   // While the GEMM CTAs stream, every global access of this CTA waits behind their requests
   // (microseconds), so all inputs are fetched in one round at the start, into shared memory:
@@ -258,7 +278,6 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
   if (tid == 0) {
     if (!s_sel) atomicOr(a.err, DEVERR_TOPK);
     if (a.count_step) *a.step = t + 1;
-    a.pack_cnt[(a.epoch + 1u) & 1u] = 0u;  // the next step's counter; this step's was cleared by the last
     __threadfence();
     st_release_u32(a.flag, a.epoch);
   }
@@ -868,10 +887,9 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
           if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         if (cand) {
-          float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc + b0);
-#pragma unroll
-          for (int i4 = 0; i4 < NH / 4; ++i4)
-            if (b0 + 4 * i4 < a.ldzc) dst[i4] = make_float4(zz[4 * i4], zz[4 * i4 + 1], zz[4 * i4 + 2], zz[4 * i4 + 3]);
+          // the candidate's row of the selected items' operand: hi parts of tokens [0, NP), then lo
+          uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
+          store_hilo<NH>(row + b0, row + NP + b0, zz);
           if (half == 0) a.scores[p] = m * n2v;
         } else if (valid) {
 #pragma unroll
@@ -911,10 +929,8 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
             if (b < a.B) m = fmaxf(m, fabsf(zz[b]));
           }
           if (cand) {
-            float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc);
-#pragma unroll
-            for (int b4 = 0; b4 < NP / 4; ++b4)
-              if (4 * b4 < a.ldzc) dst[b4] = make_float4(zz[4 * b4], zz[4 * b4 + 1], zz[4 * b4 + 2], zz[4 * b4 + 3]);
+            uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
+            store_hilo<NP>(row, row + NP, zz);
             a.scores[p] = m * n2v;
           } else {
 #pragma unroll
@@ -950,7 +966,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   __shared__ TcCtl ctl;
   __shared__ RadixScratch<TC_PROD_THREADS> rsc;
-  __shared__ int dwin[DN_WIN_WORDS];
+  __shared__ int dwin[DN_WIN_WORDS];   // per producer warp: channels of its items of DN_WIN stages
+  __shared__ int dwinp[DN_WIN_WORDS];  // the same items' positions in C (selected stages)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int SK = a.split;
@@ -968,7 +985,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   }
 
   volatile int* abort_flag = &ctl.abort_flag;
-  volatile unsigned* pack_seen = &ctl.pack_seen;
+  volatile unsigned* sel_seen = &ctl.sel_seen;
   const int unit0 = ci - a.sel, nunits = static_cast<int>(gridDim.x) / SK - a.sel;
   const int U = a.units;
   const int G = a.D / 8;  // output groups of 8 (16 bytes); a unit is a range of whole groups
@@ -982,18 +999,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   const int r0 = static_cast<int>(rank) * a.kbr / SK, r1 = (static_cast<int>(rank) + 1) * a.kbr / SK;
   const int s0 = static_cast<int>(rank) * kbs / SK, s1 = (static_cast<int>(rank) + 1) * kbs / SK;
   const int nblk = (r1 - r0) + (s1 - s0);  // stages per unit
-  // Packers of the selected items' z planes: every CTA that has units and selected blocks (npk of
-  // them); its epilogue warps pack a share as soon as the selection is out, while its producers
-  // still stream R.
-  int rws = 0, rbefore = 0;  // ranks with selected blocks; those of them before this rank
-  for (int r = 0; r < SK; ++r) {
-    const int hs = (r + 1) * kbs / SK > r * kbs / SK ? 1 : 0;
-    rws += hs;
-    if (r < static_cast<int>(rank)) rbefore += hs;
-  }
-  const int npk = min(nunits, U) * rws;
-  const int pid = unit0 * rws + rbefore;
-  const bool packer = a.sel && a.k > 0 && unit0 < U && s1 > s0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1007,7 +1012,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     }
     mbar_init(&ctl.drain, 1);
     ctl.abort_flag = 0;
-    ctl.pack_seen = a.epoch - 1u;
+    ctl.sel_seen = a.epoch - 1u;
     fence_mbar_init();
   }
   if (warp == TC_MMA_WARP) {
@@ -1046,31 +1051,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     const int h = grp & 1, ip = (grp & 3) >> 1;  // output half; item parity within the warp's pair
     const int nrs = r1 - r0;                     // R stages of each unit
     int* mywin = dwin + warp * (DN_WIN * 8);
+    int* mywinp = dwinp + warp * (DN_WIN * 8);
     int wlo = 0, whi = 0;                        // stages [wlo, whi) are in the window
     auto fill = [&](int bi0) {
       const int seg_end = bi0 < nrs ? nrs : nblk;
       wlo = bi0;
       whi = min(seg_end, bi0 + DN_WIN);
-      int c[8];
+      int c[8], ps[8];
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const int x = lane + 32 * v;
         const int bj = wlo + (x >> 3), e = x & 7;
         const int i = 2 * warp + (e & 1) + 16 * (e >> 1);  // item within its k-block
         c[v] = -1;
+        ps[v] = -1;
         if (bj < whi) {
           if (bj < nrs) {
             const int item = (r0 + bj) * TC_BK + i;
             if (item < a.nR) c[v] = __ldg(a.ch_r + item);
           } else {
             const int item = (s0 + bj - nrs) * TC_BK + i;
-            if (item < a.k) c[v] = __ldcg(a.ch_s + item);
+            if (item < a.k) {
+              c[v] = __ldcg(a.ch_s + item);
+              ps[v] = __ldcg(a.S + item);
+            }
           }
         }
       }
       __syncwarp();
 #pragma unroll
-      for (int v = 0; v < 8; ++v) mywin[lane + 32 * v] = c[v];
+      for (int v = 0; v < 8; ++v) {
+        mywin[lane + 32 * v] = c[v];
+        mywinp[lane + 32 * v] = ps[v];
+      }
       __syncwarp();
     };
     auto issue_a = [&](int bi, uint32_t sa, int d0, bool dok) {
@@ -1085,8 +1098,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
                    W2 + (nb ? static_cast<size_t>(ch) * row3 + d0 : 0), nb);
       }
     };
+    auto issue_bs = [&](int bi, uint32_t sa) {
+      // selected stage: item e of this warp's eight takes its candidate row (2 NP bf16, the hi then
+      // lo parts) as CPI 16-byte chunks; chunk c goes to column atom c / 8 (8 KB apart), 16-byte
+      // column group c % 8 of the item's 128-byte row, swizzled by the item's row within its 8
+      constexpr int CPI = NP / 4;
+#pragma unroll
+      for (int v = 0; v < CPI / 4; ++v) {
+        const int qd = lane + 32 * v;
+        const int e = qd / CPI, c = qd % CPI;
+        const int i = 2 * warp + (e & 1) + 16 * (e >> 1);
+        int p = mywinp[(bi - wlo) * 8 + e];
+        const uint32_t nb = p >= 0 ? 16u : 0u;
+        if (p >= 0 && static_cast<unsigned>(p) >= static_cast<unsigned>(a.nC)) {
+          atomicOr(a.err, DEVERR_INDEX);
+          p = 0;
+        }
+        cp_async16(sa + Cfg::A_BYTES + (c >> 3) * (TC_BK * 128) + i * 128 + (((c & 7) ^ (i & 7)) << 4),
+                   nb ? a.zcp + static_cast<size_t>(p) * (2 * NP) + 8 * c : a.zcp, nb);
+      }
+    };
     auto issue_b = [&](int bi, uint32_t sa) {
-      const int kb = bi < nrs ? r0 + bi : a.kbr + s0 + (bi - nrs);  // column block of the z planes
+      if (bi >= nrs) {
+        issue_bs(bi, sa);
+        return;
+      }
+      const int kb = r0 + bi;  // column block of the z planes
       // chunk c = pt + 256 v -> plane c / (8 NP), token row (c / 8) % NP, chunk c % 8
 #pragma unroll
       for (int v = 0; v < NP / 16; ++v) {
@@ -1109,19 +1146,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
       const bool dok = d0 < hi;
       for (int bi = 0; bi < nblk; ++bi) {
         if (bi == nrs && bi < nblk) {
-          // first selected block: the selected items' z planes of this step must be complete (the
-          // epilogue warps post it in shared memory once every packer has counted; every wait bounded)
+          // first selected block: the selection of this step must be complete. Warp 0 polls the
+          // flag in global memory and posts what it saw in shared memory; the other warps watch
+          // that (every wait bounded; no barrier across warps that a warp which gave up earlier
+          // would miss).
           int good = 1;
           if (lane == 0) {
             const uint64_t t0 = globaltimer_ns();
-            while (static_cast<int>(*pack_seen - a.epoch) < 0) {
-              if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
-                good = 0;
-                break;
+            if (warp == 0) {
+              while (static_cast<int>(ld_acquire_u32(a.flag) - a.epoch) < 0) {
+                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+                  good = 0;
+                  break;
+                }
+                __nanosleep(256);
               }
-              __nanosleep(64);
+              if (good) {
+                __threadfence_block();
+                *sel_seen = a.epoch;
+              }
+            } else {
+              while (static_cast<int>(*sel_seen - a.epoch) < 0) {
+                if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
+                  good = 0;
+                  break;
+                }
+                __nanosleep(64);
+              }
+              if (good) (void)ld_acquire_u32(a.flag);  // acquire for this warp's own reads
             }
-            if (good) (void)ld_acquire_u32(a.pack_cnt + (a.epoch & 1u));  // acquire for this warp's reads
             if (!good) fail();
           }
           good = __shfl_sync(0xffffffffu, good, 0);
@@ -1194,6 +1247,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
       const uint32_t idesc = idesc_bf16_f32(TC_BM, 2 * NP, false, true);
+      const uint32_t idesc_s = idesc_bf16_f32(TC_BM, 2 * NP, true, true);  // selected: B MN-major too
+      const int nrs = r1 - r0;
       uint32_t consumed = 0;
       int it = 0;
       bool ok = true;
@@ -1217,13 +1272,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
           fence_proxy_async();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          // descriptors once per stage: a K step of 16 items moves A by 2048 bytes (+128), B by 32 (+2)
+          // descriptors once per stage: a K step of 16 items moves A by 2048 bytes (+128), and B by 32
+          // bytes (+2) when K-major (R) or, like A, 2048 bytes when MN-major (selected items)
           const uint64_t ad = smem_desc_sw128(sa, TC_BK * 128, 1024u);
-          const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, 16u, 1024u);
-          umma_f16(d_tmem, ad, bd, idesc, bi > 0 ? 1u : 0u);
-          umma_f16(d_tmem, ad + 128, bd + 2, idesc, 1u);
-          umma_f16(d_tmem, ad + 256, bd + 4, idesc, 1u);
-          umma_f16(d_tmem, ad + 384, bd + 6, idesc, 1u);
+          if (bi < nrs) {
+            const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, 16u, 1024u);
+            umma_f16(d_tmem, ad, bd, idesc, bi > 0 ? 1u : 0u);
+            umma_f16(d_tmem, ad + 128, bd + 2, idesc, 1u);
+            umma_f16(d_tmem, ad + 256, bd + 4, idesc, 1u);
+            umma_f16(d_tmem, ad + 384, bd + 6, idesc, 1u);
+          } else {
+            const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, TC_BK * 128, 1024u);
+            umma_f16(d_tmem, ad, bd, idesc_s, bi > 0 ? 1u : 0u);
+            umma_f16(d_tmem, ad + 128, bd + 128, idesc_s, 1u);
+            umma_f16(d_tmem, ad + 256, bd + 256, idesc_s, 1u);
+            umma_f16(d_tmem, ad + 384, bd + 384, idesc_s, 1u);
+          }
           umma_commit(&ctl.empty[s]);
           ++consumed;
         }
@@ -1240,88 +1304,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const int et = threadIdx.x - 32 * TC_EPI0;
-    if (packer) {
-      // This CTA's share of the selected items, j in [j0, j1): once the selection is out, z of each
-      // (fp32, from the gate/up) split into hi / lo bf16 parts at column 64 kbr + j of the z planes,
-      // then one release count per CTA and a bounded wait until all npk packers have counted.
-      if (et == 0) {
-        int good = 1;
-        const uint64_t t0 = globaltimer_ns();
-        while (static_cast<int>(ld_acquire_u32(a.flag) - a.epoch) < 0) {
-          if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
-            good = 0;
-            break;
-          }
-          __nanosleep(256);
-        }
-        if (!good) fail();
-        ctl.epi_ok = good;
-      }
-      epi_bar();
-      const bool go = ctl.epi_ok != 0;
-      if (go && lane == 0) (void)ld_acquire_u32(a.flag);  // acquire for this warp's own reads
-      __syncwarp();
-      const unsigned up = static_cast<unsigned>(pid), un = static_cast<unsigned>(npk);
-      const int j0 = static_cast<int>(up * static_cast<unsigned>(a.k) / un);
-      const int j1 = static_cast<int>((up + 1u) * static_cast<unsigned>(a.k) / un);
-      uint16_t* zk = const_cast<uint16_t*>(a.zk);
-      const int col0 = TC_BK * a.kbr;
-      for (int c = j0; go && c < j1; c += 128) {
-        const int ncj = min(128, j1 - c);
-        if (et < ncj) {
-          int ps = __ldcg(a.S + c + et);
-          if (static_cast<unsigned>(ps) >= static_cast<unsigned>(a.nC)) {
-            atomicOr(a.err, DEVERR_INDEX);
-            ps = 0;
-          }
-          ctl.pack_pos[et] = ps;
-        }
-        epi_bar();
-        const int total = ncj * a.B;
-        for (int e0 = 0; e0 < total; e0 += 128 * 8) {
-          float zv[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int e = e0 + 128 * u + et;
-            zv[u] = e < total ? __ldcg(a.zc + static_cast<size_t>(ctl.pack_pos[e % ncj]) * a.ldzc + e / ncj) : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int e = e0 + 128 * u + et;
-            if (e < total) {
-              uint16_t h16, l16;
-              split_bf16(zv[u], h16, l16);
-              const size_t o = static_cast<size_t>(e / ncj) * a.ldk + col0 + c + e % ncj;
-              zk[o] = h16;
-              zk[a.zk_lo_off + o] = l16;
-            }
-          }
-        }
-        epi_bar();  // pack_pos is reused by the next chunk
-      }
-      __threadfence();
-      epi_bar();
-      if (et == 0 && go) {
-        unsigned* cnt = a.pack_cnt + (a.epoch & 1u);
-        __threadfence();  // with the barrier: every epilogue thread's planes before the count
-        atomicAdd(cnt, 1u);
-        int good = 1;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_u32(cnt) < un) {
-          if (*abort_flag || globaltimer_ns() - t0 > a.wait_ns) {
-            good = 0;
-            break;
-          }
-          __nanosleep(128);
-        }
-        if (good) {
-          __threadfence_block();
-          *pack_seen = a.epoch;
-        } else {
-          fail();
-        }
-      }
-    }
     int it = 0;
     for (int unit = unit0; unit < U; unit += nunits, ++it) {
       const int buf = it & 1;
@@ -1506,7 +1488,7 @@ template <int NP>
 cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   // the ring, or the selecting CTA's keys (|C| of them) if those need more
   size_t smem = dn_smem_bytes<NP>();
-  constexpr size_t kStatic = sizeof(TcCtl) + sizeof(RadixScratch<TC_PROD_THREADS>) + sizeof(int) * DN_WIN_WORDS + 64;
+  constexpr size_t kStatic = sizeof(TcCtl) + sizeof(RadixScratch<TC_PROD_THREADS>) + 2 * sizeof(int) * DN_WIN_WORDS + 64;
   constexpr size_t kMaxDyn = 227 * 1024 - kStatic;
   const size_t c16 = (static_cast<size_t>(a.nC) * 4 + 15) & ~size_t(15);
   const size_t keys_bytes = 1024 + c16;

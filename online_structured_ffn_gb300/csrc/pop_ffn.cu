@@ -43,6 +43,7 @@ struct pop_ffn {
   uint16_t* zk = nullptr;  // [2][max_batch][ldk]: bf16 hi and lo parts of z of the kept items (R, then S)
   int ldk = 0;
   int* ch_s = nullptr;     // channels of the selected candidates, in S order
+  uint16_t* zcp = nullptr; // [N][2 * round_up(max_batch, 16)]: the candidates' z rows (hi, lo), B > 1
   // B > 1 decode slabs (rebuilt at every partition): gate/up rows of R u C and down columns of R
   GuSlabGeom gu_geom{};
   uint16_t* gu_slab = nullptr;
@@ -64,8 +65,8 @@ struct pop_ffn {
 };
 
 static constexpr int kProfEvents = 5;
-// device counters: [4] candidates scored by the B = 1 gate/up, [5] the B > 1 selection flag, [6, 7]
-// the B > 1 pack counters, [8..] tiles of y done by the B = 1 down chunks
+// device counters: [4] candidates scored by the B = 1 gate/up, [5] the B > 1 selection flag, [8..]
+// tiles of y done by the B = 1 down chunks
 static constexpr int kSyncWords = 64;
 static constexpr int kProfMaxSteps = 256;
 
@@ -125,7 +126,7 @@ void prof_end(pop_ffn* h) {
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
                   h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_s,
-                  h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab};
+                  h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab, h->zcp};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -184,8 +185,7 @@ pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st) {
   a.nC = h->cnt.n_C;
   a.nR = h->cnt.n_R;
   a.n2 = h->n2;
-  a.zc = h->z;
-  a.ldzc = round_up(B, 4);
+  a.zcp = h->zcp;
   a.zk = h->zk;
   a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
   a.ldk = h->ldk;
@@ -252,8 +252,7 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.dslab = decode ? h->dn_slab : nullptr;
   a.sel = decode && h->cnt.n_C > 0 ? 1 : 0;
   a.scores = h->scores;
-  a.zc = h->z;
-  a.ldzc = round_up(B, 4);
+  a.zcp = h->zcp;
   a.rc = h->rc;
   a.nC = h->cnt.n_C;
   a.period = h->cfg.period;
@@ -263,7 +262,6 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.count_step = decode ? 1 : 0;
   a.flag = h->fsync + 5;
   a.epoch = decode ? ++h->epoch : 0;
-  a.pack_cnt = h->fsync + 6;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   POP_CUDA(h, launch_down_tc(a, h->num_sms, st));
@@ -387,6 +385,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   if (cfg->max_batch > 1) {
     POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
     POP_ALLOC(h->ch_s, N);
+    POP_ALLOC(h->zcp, static_cast<size_t>(N) * 2 * round_up(cfg->max_batch, 16));
     h->gu_geom = gu_slab_geom(cnt.n_C + cnt.n_R, D, h->num_sms);
     POP_ALLOC(h->gu_slab, gu_slab_elems(h->gu_geom));
     POP_ALLOC(h->dn_slab, dn_slab_elems(D, cnt.n_R));

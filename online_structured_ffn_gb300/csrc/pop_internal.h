@@ -66,8 +66,7 @@ struct DownTcArgs {
   // selection by the first cluster (sel = 1, decode with candidates)
   int sel;
   const float* scores;   // [nC] this step's candidate scores
-  const float* zc;       // [nC][ldzc] candidates' z
-  int ldzc;
+  const uint16_t* zcp;   // [nC][2 NP] candidates' z rows (hi, lo) from the gate/up
   const int* rc;         // position -> channel, C first
   int nC, period;
   float* memory;
@@ -76,8 +75,6 @@ struct DownTcArgs {
   int count_step;        // 1: advance the step counter (decode)
   unsigned* flag;        // selection of step `epoch` complete when *flag == epoch
   unsigned epoch;
-  unsigned* pack_cnt;    // [2], by epoch parity: producer warps that have packed their share of the
-                         // selected items' z planes this step (the selecting CTA clears the other one)
   // work split (set by the launcher)
   int split, units;
   unsigned* err;
@@ -112,8 +109,8 @@ struct GateUpSlabArgs {
   const int* rc;         // for the candidates' down-column norms
   int nC, nR;
   const float* n2;
-  float* zc;             // out, as GateUpTcArgs
-  int ldzc;
+  uint16_t* zcp;         // out: the candidates' z rows, [nC][2 NP] bf16 (hi parts of the NP tokens,
+                         // then their lo parts), the down GEMM's MN-major operand for selected items
   uint16_t* zk;
   uint16_t* zk_lo;
   int ldk;
