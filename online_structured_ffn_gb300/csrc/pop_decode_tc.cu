@@ -198,6 +198,14 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
+__device__ __forceinline__ float4 ld_peer4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ float2 ld_peer2(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
@@ -957,6 +965,50 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
   }
 }
 
+// One epilogue thread's part of a split unit's reduction: the NP / SK tokens [b0, b0 + NP / SK) of
+// one output row d, from the partial rows of all SK CTAs of the cluster (16-byte distributed
+// shared-memory reads, all issued before the first add), added in rank order and stored to y.
+template <int NP, int SK>
+__device__ __forceinline__ void cluster_finish_row(const DownTcArgs& a, uint32_t pbase, int b0, int d, bool dok) {
+  constexpr int TPT = NP / SK;
+  static_assert(TPT % 2 == 0, "tokens per thread");
+  constexpr int W = TPT % 4 == 0 ? 4 : 2;  // floats per load
+  constexpr int L = TPT / W;               // loads per peer
+  float v[SK][TPT];
+#pragma unroll
+  for (int pr = 0; pr < SK; ++pr) {
+    const uint32_t base = map_peer(pbase, static_cast<uint32_t>(pr)) + 4u * b0;
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      if (W == 4) {
+        const float4 t = ld_peer4(base + 16u * l);
+        v[pr][4 * l] = t.x;
+        v[pr][4 * l + 1] = t.y;
+        v[pr][4 * l + 2] = t.z;
+        v[pr][4 * l + 3] = t.w;
+      } else {
+        const float2 t = ld_peer2(base + 8u * l);
+        v[pr][2 * l] = t.x;
+        v[pr][2 * l + 1] = t.y;
+      }
+    }
+  }
+  if (!dok) return;
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) {
+    float g = 0.f;
+#pragma unroll
+    for (int pr = 0; pr < SK; ++pr) g += v[pr][j];
+    const int bb = b0 + j;
+    if (bb < a.B) {
+      if (a.out_f32)
+        static_cast<float*>(a.y)[static_cast<size_t>(bb) * a.D + d] = g;
+      else
+        static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(bb) * a.D + d] = __float2bfloat16_rn(g);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ selection + down over R u S
 template <int NP>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant__ DownTcArgs a) {
@@ -1368,38 +1420,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
       const int d = unit_lo(unit0) + row;
       const bool dok = d < unit_lo(unit0 + 1);
       const uint32_t pbase = smem_u32(smem) + static_cast<uint32_t>(row * NP) * 4u;
-      uint32_t peer[8];
-#pragma unroll
-      for (int pr = 0; pr < 8; ++pr) peer[pr] = pr < SK ? map_peer(pbase, static_cast<uint32_t>(pr)) : 0u;
-      // tokens two at a time (tpt = NP / SK is even): SK peers x 8-byte loads, added in rank order
-#pragma unroll 2
-      for (int jj = 0; jj < tpt; jj += 2) {
-        const int b = b0 + jj;
-        float2 lg[8];
-#pragma unroll
-        for (int pr = 0; pr < 8; ++pr)
-          if (pr < SK) lg[pr] = ld_peer2(peer[pr] + 4u * b);
-        float2 g2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int pr = 0; pr < 8; ++pr) {
-          if (pr < SK) {
-            g2.x += lg[pr].x;
-            g2.y += lg[pr].y;
-          }
-        }
-        if (dok) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int bb = b + hh;
-            const float g = hh ? g2.y : g2.x;
-            if (bb < a.B) {
-              if (a.out_f32)
-                static_cast<float*>(a.y)[static_cast<size_t>(bb) * a.D + d] = g;
-              else
-                static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(bb) * a.D + d] = __float2bfloat16_rn(g);
-            }
-          }
-        }
+      switch (SK) {
+        case 2: cluster_finish_row<NP, 2>(a, pbase, b0, d, dok); break;
+        case 4: cluster_finish_row<NP, 4>(a, pbase, b0, d, dok); break;
+        default: cluster_finish_row<NP, 8>(a, pbase, b0, d, dok); break;
       }
     }
     cluster_sync_all();  // no CTA leaves while a peer may still read its partials
