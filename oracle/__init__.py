@@ -56,6 +56,12 @@ Readings where the pages are silent or garbled (each repeated at its function):
    and memory; an expert that receives no token in a step scores each
    candidate 0 (the maximum of non-negative values over no tokens) and
    contributes no output.
+8. Periodic "skip" variant (the [BWAP] abstract's periodic top-k read so that
+   the mask's saving reaches the gate/up too): at update steps (t mod P == 0)
+   the step is the full one above; in between, gate/up runs only over R and
+   the held selection S, the memory gains the scores of S only (the other
+   candidates are not computed) and y is the same sum over R u S. P = 1 is
+   per-step POP.
 """
 from __future__ import annotations
 
@@ -242,6 +248,7 @@ class PopSession:
     C: np.ndarray
     k: int
     period: int = 1
+    skip: bool = False   # reading 8: between updates, gate/up only over R u S
     t: int = 0
     memory: np.ndarray = field(default=None)
     S: np.ndarray = field(default=None)          # selected candidate positions (into C), ascending
@@ -263,6 +270,8 @@ class PopSession:
 
     def step(self, x) -> np.ndarray:
         x = _f64(x)
+        if self.skip and self.t % self.period != 0:
+            return self._skip_step(x)
         RC = np.concatenate([self.C, self.R])
         # H_t = f(X_t; R u C): gate/up only over the retained and candidate rows
         Z_RC = ffn_activations(self.Wg[RC], self.W1[RC], x)
@@ -279,6 +288,22 @@ class PopSession:
         keep = np.sort(np.concatenate([self.R, self.C[self.S]]))
         Z_full = np.zeros((x.shape[0], self.W2.shape[1]))
         Z_full[:, RC] = Z_RC
+        return down_projection(self.W2, Z_full, keep)
+
+    def _skip_step(self, x) -> np.ndarray:
+        """A step between updates of the skip variant (reading 8): z over R and the held S only."""
+        CS = self.C[self.S]
+        RS = np.concatenate([CS, self.R])
+        Z_RS = ffn_activations(self.Wg[RS], self.W1[RS], x)
+        a_S = candidate_scores(Z_RS[:, :CS.shape[0]], self.n2_C[self.S])
+        self.memory[self.S] = self.memory[self.S] + a_S
+        self.last_scores = np.zeros(self.C.shape[0])
+        self.last_scores[self.S] = a_S
+        self.last_z = Z_RS
+        self.t += 1
+        keep = np.sort(np.concatenate([self.R, CS]))
+        Z_full = np.zeros((x.shape[0], self.W2.shape[1]))
+        Z_full[:, RS] = Z_RS
         return down_projection(self.W2, Z_full, keep)
 
     def kept_channels(self) -> np.ndarray:

@@ -493,3 +493,45 @@ def test_moe_decode_expert_major_equals_stepping_the_layer():
         for e in range(E):
             s = sess.sessions[e]
             assert per[e][t]["S"].tolist() == s.C[s.S].tolist()
+
+
+# ----------------------------------------------------------------- periodic skip variant (reading 8)
+
+def _skip_pair(period, seed=50, D=12, N=60, B=3):
+    Wg, W1, W2 = _tiny_layer(seed, D, N)
+    pre = oracle.prefill(Wg, W1, W2, _x(seed, 10, D), r=0.3, gamma=0.1)
+    k = pre["counts"].k
+    full = oracle.PopSession(Wg, W1, W2, pre["R"], pre["C"], k, period=period)
+    skip = oracle.PopSession(Wg, W1, W2, pre["R"], pre["C"], k, period=period, skip=True)
+    xs = [_x(seed, B, D, step=t) for t in range(3 * period + 1)]
+    return full, skip, xs
+
+
+def test_skip_with_period_one_is_per_step_pop():
+    full, skip, xs = _skip_pair(1)
+    for x in xs:
+        np.testing.assert_array_equal(skip.step(x), full.step(x))
+        assert skip.S.tolist() == full.S.tolist()
+
+
+def test_skip_steps_give_the_held_mask_output_and_memory_of_s_only():
+    # until the first update after t = 0 both variants hold the same S, so y agrees; the skip
+    # variant's memory is the full variant's per-step scores summed over those steps, on S only
+    P = 4
+    full, skip, xs = _skip_pair(P)
+    acc = np.zeros(full.C.shape[0])
+    for t in range(P):
+        y_full, y_skip = full.step(xs[t]), skip.step(xs[t])
+        np.testing.assert_allclose(y_skip, y_full, rtol=1e-12, atol=1e-14)
+        if t > 0:
+            acc += full.last_scores
+    mask = np.zeros(full.C.shape[0], dtype=bool)
+    mask[skip.S] = True
+    np.testing.assert_allclose(skip.memory, np.where(mask, acc, 0.0), rtol=1e-12, atol=1e-15)
+    # the update step selects from the memory plus this step's full scores, by the top-k rule
+    skip.step(xs[P])
+    full.step(xs[P])
+    a = full.last_scores
+    expect = oracle.select_topk(np.where(mask, acc, 0.0) + a, full.k)
+    assert skip.S.tolist() == expect.tolist()
+    np.testing.assert_array_equal(skip.memory, np.zeros_like(skip.memory))
