@@ -44,6 +44,16 @@ WORKLOADS = {
                               chunk=4096),
     "llama-70b-ffn-b64-p16": dict(D=8192, N=28672, r=0.5, gamma=0.1, B=64, M=64 * 512, T=1024, period=16,
                                   layers=1, chunk=8192),
+    # the same with the periodic skip variant: between updates gate/up only over R and the held selection
+    "llama-70b-ffn-b64-p16-skip": dict(D=8192, N=28672, r=0.5, gamma=0.1, B=64, M=64 * 512, T=1024, period=16,
+                                       layers=1, chunk=8192, skip=True),
+    # the POP notes' ablation comparators on the 7B B=1 workload: a static mask (gamma = 0: no
+    # candidates, the prefill's top-keep every step) and full per-step re-evaluation (gamma >=
+    # max(r, 1 - r): every channel a candidate, a top-keep over all of them every step)
+    "llama2-7b-ffn-b1-static": dict(D=4096, N=11008, r=0.299, gamma=0.0, B=1, M=2048, T=256, period=1, layers=4,
+                                    chunk=2048),
+    "llama2-7b-ffn-b1-fulldyn": dict(D=4096, N=11008, r=0.299, gamma=0.701, B=1, M=2048, T=256, period=1,
+                                     layers=4, chunk=2048),
     # MoE layer: 8 experts of D=4096, D_FF=14336, top-2 routing, prompt of 8 sequences x 512 tokens
     "moe-8x4096x14336-b32": dict(D=4096, N=14336, r=0.3, gamma=0.1, B=32, M=8 * 512, T=128, period=1, layers=1,
                                  chunk=2048, experts=8),
@@ -66,9 +76,15 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def touched_bytes(c, D):
-    """Algorithmic weight bytes of one decode step: gate+up rows over R u C, down columns over R u S."""
-    gateup = 2 * (c.n_R + c.n_C) * D * 2
+def touched_bytes(c, D, wl=None):
+    """Algorithmic weight bytes of one decode step: gate+up rows over R u C, down columns over R u S.
+    With the periodic skip variant the gate/up rows are R u C on update steps and R u S in between:
+    the average over a period."""
+    rows = c.n_R + c.n_C
+    if wl is not None and wl.get("skip") and wl["period"] > 1 and c.n_C > 0:
+        P = wl["period"]
+        rows = ((c.n_R + c.n_C) + (P - 1) * (c.n_R + c.k)) / P
+    gateup = 2 * rows * D * 2
     down = c.keep * D * 2
     return gateup, down
 
@@ -197,7 +213,7 @@ class Stack:
             tg, t1, t2 = up(Wg), up(W1), up(W2)
             del Wg, W1, W2
             f = pop.PopFFN(tg, t1, t2, r=wl["r"], gamma=wl["gamma"], period=wl["period"], max_batch=B,
-                           max_prefill_tokens=wl["chunk"], out_f32=True)
+                           max_prefill_tokens=wl["chunk"], out_f32=True, skip=wl.get("skip", False))
             torch.cuda.synchronize()
             del tg, t1, t2
             self.ffn.append(f)
@@ -414,12 +430,13 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
         f.profile(False)
         f.check()
     B, T, Lyr = wl["B"], wl["T"], wl["layers"]
+    dense_us = dense_step_us(stack) if not wl.get("experts") else None
     units = B * T * Lyr * steps
     g_elapsed, g_units = aggregate(elapsed, units, device=torch.device("cuda", torch.cuda.current_device()))
     ksum = [sum(p[0][i] for p in prof) for i in range(4)]
     nsteps = sum(p[1] for p in prof)
     c = stack.counts
-    gu_bytes, dn_bytes = touched_bytes(c, wl["D"])
+    gu_bytes, dn_bytes = touched_bytes(c, wl["D"], wl)
     nexp = wl.get("experts", 1)  # every expert streams its weights every step
     peak, peak_kind = measured_peaks()
     gu_ms = ksum[0] / max(nsteps, 1)
@@ -428,7 +445,7 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     res = dict(
         value=g_units / g_elapsed, elapsed=g_elapsed, units=g_units, ms_per_step=1e3 * g_elapsed / steps,
         decode_only_tokens_per_s=B * T * Lyr * steps / dec_s,
-        decode_step_us=1e6 * dec_step_s,
+        decode_step_us=1e6 * dec_step_s, dense_step_us=dense_us,
         prefill_ms_per_layer=1e3 * (elapsed - dec_s) / (steps * Lyr),
         kernel_us={n: 1e3 * ksum[i] / max(nsteps, 1) for i, n in enumerate(("gateup", "select", "down", "reduce"))},
         roof_bytes=roof_bytes,
@@ -445,6 +462,35 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     del stack
     torch.cuda.empty_cache()
     return res
+
+
+def dense_step_us(stack, reps=2):
+    """The dense FFN (pop_ffn_dense_ref: every channel, the same kernels' dense path) on the same
+    decode inputs, through every layer: microseconds per decode step, for comparison."""
+    import torch
+    pop, wl = stack.pop, stack.wl
+    lib = pop.load_library()
+    st = torch.cuda.current_stream().cuda_stream
+    B, T, D = wl["B"], wl["T"], wl["D"]
+    xs, ys = stack.x.view(-1, D), stack.y.view(-1, D)
+
+    def one():
+        i = 0
+        for _ in range(T):
+            for f in stack.ffn:
+                s = lib.pop_ffn_dense_ref(f.handle, xs[i * B].data_ptr(), B, ys[i * B].data_ptr(), st)
+                if s:
+                    pop._check(s, f.handle)
+                i += 1
+    one()  # warm
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    return 1e3 * e0.elapsed_time(e1) / (reps * T * len(stack.ffn))
 
 
 def run_e2e(stack, steps):
@@ -586,7 +632,8 @@ def main():
         WORKLOADS[args.workload] = dict(WORKLOADS[args.workload], T=args.decode_steps)
     wl = WORKLOADS[args.workload]
     moe_keys = {"experts": wl["experts"], "routing": "top-2"} if wl.get("experts") else {}
-    config = {"workload": args.workload, **moe_keys, "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
+    config = {"workload": args.workload, **moe_keys, **({"skip": True} if wl.get("skip") else {}),
+              "D": wl["D"], "D_FF": wl["N"], "r": wl["r"], "gamma": wl["gamma"],
               "B": wl["B"], "prompt_tokens": wl["M"], "decode_steps": wl["T"], "period": wl["period"],
               "layers": wl["layers"],
               "l2": ("inputs larger than L2: each decode step streams every expert's weights "
@@ -636,7 +683,8 @@ def main():
                      "decode_only_tokens_per_s": s["decode_only_tokens_per_s"],
                      "decode_step_us": s["decode_step_us"], "kernel_us": s["kernel_us"],
                      "gateup_hbm_gbs": s["gateup_gbs"], "gateup_frac": s["gateup_gbs"] / s["peak"],
-                     "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"]}
+                     "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"],
+                     "dense_step_us": s["dense_step_us"]}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -656,6 +704,9 @@ def main():
                      "frac": res["gateup_gbs"] / res["peak"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": res["roof_bytes"], "peak_source": res["peak_kind"]},
         "decode_step": {"us": res["decode_step_us"], "hbm_gbs": res["step_gbs"], "frac": res["step_gbs"] / res["peak"],
+                        "dense_us": res["dense_step_us"],
+                        "speedup_vs_dense": (res["dense_step_us"] / res["decode_step_us"]
+                                             if res["dense_step_us"] else None),
                         "touched_bytes": res["experts"] * (res["gu_bytes"] + res["dn_bytes"]),
                         "kernel_us": res["kernel_us"],
                         "tokens_per_s": res["decode_only_tokens_per_s"]},

@@ -77,6 +77,9 @@ typedef struct {
   int max_batch;          /* largest B accepted by pop_decode_step, 1..POP_MAX_BATCH. */
   int max_prefill_tokens; /* prefill chunk: longer prompts run in chunks of this many tokens. >= 1. */
   int out_f32;            /* dtype of y / Y: 1 = float32, 0 = bf16. */
+  int skip;               /* periodic skip variant (0 or 1; takes effect with period > 1): between
+                             updates gate/up runs only over R and the held selection, and the memory
+                             gains the scores of the held selection only. 0 = off. */
 } pop_config;
 
 typedef struct {

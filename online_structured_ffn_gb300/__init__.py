@@ -25,7 +25,7 @@ POP_MAX_D, POP_MAX_D_FF, POP_MAX_BATCH, POP_STATIC_MAX_D_FF = 16384, 49152, 64, 
 class pop_config(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int), ("D_FF", ctypes.c_int), ("r", ctypes.c_double), ("gamma", ctypes.c_double),
                 ("period", ctypes.c_int), ("max_batch", ctypes.c_int), ("max_prefill_tokens", ctypes.c_int),
-                ("out_f32", ctypes.c_int)]
+                ("out_f32", ctypes.c_int), ("skip", ctypes.c_int)]
 
 
 class pop_counts(ctypes.Structure):
@@ -257,11 +257,12 @@ class PopFFN:
     """
 
     def __init__(self, Wg, W1, W2, r: float, gamma: float = 0.1, period: int = 1, max_batch: int = 1,
-                 max_prefill_tokens: int = 2048, out_f32: bool = True, stream=None):
+                 max_prefill_tokens: int = 2048, out_f32: bool = True, skip: bool = False, stream=None):
         N, D = Wg.shape
         self.handle = None
         self.cfg = pop_config(D=D, D_FF=N, r=r, gamma=gamma, period=period, max_batch=max_batch,
-                              max_prefill_tokens=max_prefill_tokens, out_f32=1 if out_f32 else 0)
+                              max_prefill_tokens=max_prefill_tokens, out_f32=1 if out_f32 else 0,
+                              skip=1 if skip else 0)
         self.D, self.N = D, N
         self.handle = pop_ffn_create(self.cfg, Wg, W1, W2, stream)
         self.counts = pop_ffn_counts(self.handle)

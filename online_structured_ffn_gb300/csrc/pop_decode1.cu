@@ -107,13 +107,37 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
         s_ok = ok;
       }
       __syncthreads();
-      if (s_ok) {
+      if (s_ok && a.skip) {
+        // skip variant between updates: the candidates scored are the held selection (position j
+        // of this step's list is S_hold[j]); their scores join the memory, nothing is selected
+        const int t = *a.step;
+        for (int j = threadIdx.x; j < a.nC; j += GS_THREADS) {
+          int ps = __ldg(a.S_hold + j);
+          if (static_cast<unsigned>(ps) >= static_cast<unsigned>(a.N)) {
+            atomicOr(a.err, DEVERR_INDEX);
+            ps = 0;
+          }
+          a.memory[ps] += __ldcg(a.scores + j);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) *a.step = t + 1;
+      } else if (s_ok) {
         uint32_t* keys = reinterpret_cast<uint32_t*>(xs);
         const int t = *a.step;
+        const bool update = (t % a.period) == 0;
         const bool sel = select_step<GS_THREADS>(
-            threadIdx.x, [&](int i) { return __ldcg(a.scores + i); }, a.memory, a.nC, a.k, a.period,
-            (t % a.period) == 0, keys, a.S, sc, BlockSync256());
+            threadIdx.x, [&](int i) { return __ldcg(a.scores + i); }, a.memory, a.nC, a.k, a.period, update, keys,
+            a.S, sc, BlockSync256());
         __syncthreads();
+        if (a.rcs && update)  // skip variant: the next steps' list starts with the selected channels
+          for (int j = threadIdx.x; j < a.k; j += GS_THREADS) {
+            int ps = a.S[j];
+            if (static_cast<unsigned>(ps) >= static_cast<unsigned>(a.nC)) {
+              atomicOr(a.err, DEVERR_INDEX);
+              ps = 0;
+            }
+            a.rcs[j] = a.rc[ps];
+          }
         if (threadIdx.x == 0) {
           if (!sel) atomicOr(a.err, DEVERR_TOPK);
           *a.step = t + 1;
@@ -136,11 +160,12 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
   const int r0 = rb0 + warp * (rb1 - rb0) / GS_WARPS, r1 = rb0 + (warp + 1) * (rb1 - rb0) / GS_WARPS;
   const int nch = D >> 3;
   const size_t row3 = 3 * static_cast<size_t>(D);
-  // constant data only before the wait: warm L2 with this warp's first channel
+  // constant data only before the wait: warm L2 with this warp's first channel (on a skip step
+  // the list's head, the held selection, may be written by the kernel before: R only)
   {
-    const int p = c0 < c1 ? c0 : (r0 < r1 ? r0 : -1);
+    const int p = c0 < c1 && !a.skip ? c0 : (r0 < r1 ? r0 : -1);
     if (p >= 0) {
-      const int ch = a.rc[p];
+      const int ch = __ldcg(a.rc + p);
       if (static_cast<unsigned>(ch) < static_cast<unsigned>(a.N)) {
         const uint8_t* row = reinterpret_cast<const uint8_t*>(a.Wp + static_cast<size_t>(ch) * row3);
         for (int off = lane * 128; off < 4 * D; off += 32 * 128) prefetch_l2(row + off);
@@ -158,7 +183,7 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
   constexpr int GRP = NCHL < 4 ? NCHL : 4;
 
   auto item = [&](int p) {
-    const int ch = guard_idx(a.rc[p], a.N, a.err);
+    const int ch = guard_idx(__ldcg(a.rc + p), a.N, a.err);
     const uint16_t* rg = a.Wp + static_cast<size_t>(ch) * row3;
     const uint16_t* ru = rg + D;
     float ag0 = 0.f, ag1 = 0.f, au0 = 0.f, au1 = 0.f;
@@ -266,11 +291,11 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
     for (int e = threadIdx.x; e < cnt; e += DT_THREADS) {
       const int it = base + e;
       if (it < nr) {
-        if (!first) s_ch[e] = guard_idx(a.rc[a.nC + r_lo + it], a.N, a.err);
+        if (!first) s_ch[e] = guard_idx(__ldcg(a.rc + a.nC + r_lo + it), a.N, a.err);
         s_z[e] = a.z[a.nC + r_lo + it];
       } else {
         const int pos = guard_idx(a.S[s_lo + it - nr], a.nC, a.err);
-        s_ch[e] = guard_idx(a.rc[pos], a.N, a.err);
+        s_ch[e] = guard_idx(__ldcg(a.rc + pos), a.N, a.err);
         s_z[e] = a.z[pos];
       }
     }
@@ -374,13 +399,13 @@ static bool split_fits(long long parts, long long items) { return parts * items 
 cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st) {
   if (!split_fits(grid, a.nC > a.nR ? a.nC : a.nR)) return cudaErrorInvalidValue;
   const int nchl = pow2_ceil((a.D / 8 + 31) / 32);
-  const size_t keys = a.do_select ? static_cast<size_t>(a.nC > 0 ? a.nC : 1) * sizeof(uint32_t) : 0;
+  const size_t keys = a.do_select && !a.skip ? static_cast<size_t>(a.nC > 0 ? a.nC : 1) * sizeof(uint32_t) : 0;
   const size_t xsz = static_cast<size_t>(a.D) * sizeof(float);
   const size_t smem = keys > xsz ? keys : xsz;
 #define POP_GS(NC)                                                                                              \
   case NC: {                                                                                                    \
     static size_t configured = 0;                                                                               \
-    if (smem > 48 * 1024 && smem > configured) {                                                                \
+    if (smem > configured) {  /* the static scratch counts toward the 48 KB default too */                    \
       cudaError_t e = cudaFuncSetAttribute(k_gateup_sel_b1<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                                            static_cast<int>(smem));                                             \
       if (e != cudaSuccess) return e;                                                                           \

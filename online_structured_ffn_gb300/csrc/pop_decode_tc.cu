@@ -55,6 +55,8 @@
 // DEVERR_TIMEOUT_DECODE_TC, stops issuing, drains its own copies and MMAs (bounded), frees TMEM and
 // returns. The warps of a role take every decision that guards a named barrier together, and every
 // thread reaches the cluster barriers, so a time-out cannot leave a barrier waiting.
+#include <algorithm>
+
 #include "pop_device.cuh"
 #include "pop_internal.h"
 #include "pop_radix.cuh"
@@ -223,6 +225,25 @@ struct ProdSync {
 // advances the step counter and releases the flag. The GEMM CTAs then gather the selected items'
 // z straight from the gate/up's candidate rows (an MN-major operand), so nothing is packed here.
 __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_PROD_THREADS>& rsc) {
+  if (a.skip) {
+    // skip variant between updates: positions [0, k) of this step's list are the held selection
+    // S_hold; their scores join the memory, the selection and its channels stay as they are
+    for (int j = threadIdx.x; j < a.k; j += TC_THREADS) {
+      int ps = __ldg(a.S_hold + j);
+      if (static_cast<unsigned>(ps) >= static_cast<unsigned>(a.N)) {
+        atomicOr(a.err, DEVERR_INDEX);
+        ps = 0;
+      }
+      a.memory[ps] += __ldcg(a.scores + j);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (a.count_step) *a.step += 1;
+      __threadfence();
+      st_release_u32(a.flag, a.epoch);
+    }
+    return;
+  }
   // While the GEMM CTAs stream, every global access of this CTA waits behind their requests
   // (microseconds), so all inputs are fetched in one round at the start, into shared memory:
   //   [keys: nC u32 | scores: nC f32 | channels of C: nC i32 | S: k i32 | memory: nC f32 (period > 1)]
@@ -280,7 +301,9 @@ __device__ void down_select(const DownTcArgs& a, uint8_t* smem, RadixScratch<TC_
       sS[j] = 0;
       if (update && small) a.S[j] = 0;
     }
-    a.ch_s[j] = guard_ch(small ? s_rc[ps] : __ldg(a.rc + ps), a.N, a.err);
+    const int ch = guard_ch(small ? s_rc[ps] : __ldg(a.rc + ps), a.N, a.err);
+    a.ch_s[j] = ch;
+    if (a.rcs && update) a.rcs[j] = ch;  // skip variant: the list of the steps until the next update
   }
   __syncthreads();
   if (tid == 0) {
@@ -370,6 +393,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int u = 0; u < KS; ++u)
         tma_load_2d(smem + s * STAGE + u * SUB + AROWS * 128, &mapX, &ctl.full[s], (sbk * KS + u) * TC_BK, 0);
     };
+    if (a.list_after_wait) pdl_wait();  // the list itself is this step's data
     for (int u = w; u < U && ok; u += W) {
       const int lo = unit_lo(u), nrows = unit_lo(u + 1) - lo;
       uint32_t rowbase[4], dst[4];
@@ -380,7 +404,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         dst[t] = 0u;
         if (rr < 2 * nrows) {
           const int g = rr & 1, j = rr >> 1;
-          const int ch = guard_ch(__ldg(a.rc + lo + j), a.N, a.err);
+          const int ch = guard_ch(a.list_after_wait ? __ldcg(a.rc + lo + j) : __ldg(a.rc + lo + j), a.N, a.err);
           const int arow = 32 * (j >> 4) + 16 * g + (j & 15);
           rowbase[t] = static_cast<uint32_t>(ch) * row3 + static_cast<uint32_t>(g) * a.D + 8 * cq;
           dst[t] = arow * 128 + ((cq ^ (arow & 7)) << 4);
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const bool cand = valid && p < a.nC;
       // the candidates' down-column norms, fetched while the accumulators are still being built
       float n2v = 0.f;
-      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldg(a.rc + p), a.N, a.err));
+      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldcg(a.rc + p), a.N, a.err));
       if (et == 0)
         ctl.seg_ok[buf] = mbar_wait_bounded(&ctl.tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
       epi_bar();
@@ -552,10 +576,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
       if (cand) {
-        float4* dst = reinterpret_cast<float4*>(a.zc + static_cast<size_t>(p) * a.ldzc + b0);
-#pragma unroll
-        for (int i4 = 0; i4 < NH / 4; ++i4)
-          if (b0 + 4 * i4 < a.ldzc) dst[i4] = make_float4(zz[4 * i4], zz[4 * i4 + 1], zz[4 * i4 + 2], zz[4 * i4 + 3]);
+        uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
+        store_hilo<NH>(row + b0, row + NP + b0, zz);
         if (half == 0) a.scores[p] = m * n2v;
       } else if (valid) {
 #pragma unroll
@@ -590,18 +612,21 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* src, uint32
 
 // One 16-byte chunk per thread (grid-stride): chunk e of the gate/up slab is position pos = e % 8 of
 // A row ar of k-block kb of tile t; it holds data chunk c = pos ^ (ar % 8) (the 128-byte swizzle).
+// IDX is the index type: 32-bit when the chunk count allows it (64-bit division is slow here).
+template <class IDX>
 __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __restrict__ rc, int D, int N,
                                 GuSlabGeom g, uint16_t* __restrict__ slab, unsigned* __restrict__ err) {
-  const size_t total = static_cast<size_t>(g.T) * g.KB * g.arows * 8;
+  const IDX total = static_cast<IDX>(g.T) * g.KB * g.arows * 8;
   const int grows = (g.RT + 7) / 8 * 8;
-  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+  const IDX arows = static_cast<IDX>(g.arows), KB = static_cast<IDX>(g.KB);
+  for (IDX e = static_cast<IDX>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<IDX>(gridDim.x) * blockDim.x) {
     const int pos = static_cast<int>(e & 7);
-    size_t rest = e >> 3;
-    const int ar = static_cast<int>(rest % g.arows);
-    rest /= g.arows;
-    const int kb = static_cast<int>(rest % g.KB);
-    const int t = static_cast<int>(rest / g.KB);
+    IDX rest = e >> 3;
+    const int ar = static_cast<int>(rest % arows);
+    rest /= arows;
+    const int kb = static_cast<int>(rest % KB);
+    const int t = static_cast<int>(rest / KB);
     const int c = pos ^ (ar & 7);
     int j, gu;
     if (g.paired) {
@@ -616,14 +641,14 @@ __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __re
     const int d = kb * TC_BK + 8 * c;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (j < g.RT && p < g.P && d < D) {
-      int ch = rc[p];
+      int ch = __ldcg(rc + p);
       if (static_cast<unsigned>(ch) >= static_cast<unsigned>(N)) {
         atomicOr(err, DEVERR_INDEX);
         ch = 0;
       }
-      v = *reinterpret_cast<const uint4*>(Wp + static_cast<size_t>(ch) * 3 * D + static_cast<size_t>(gu) * D + d);
+      v = ldg_stream(Wp + static_cast<size_t>(ch) * 3 * D + static_cast<size_t>(gu) * D + d);
     }
-    *reinterpret_cast<uint4*>(slab + e * 8) = v;
+    *reinterpret_cast<uint4*>(slab + static_cast<size_t>(e) * 8) = v;
   }
 }
 
@@ -856,7 +881,7 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
       const bool cand = valid && p < a.nC;
       const int half = PAIRED ? (lane >> 4) : 0;
       float n2v = 0.f;
-      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldg(a.rc + p), a.N, a.err));
+      if (cand && half == 0) n2v = __ldg(a.n2 + guard_ch(__ldcg(a.rc + p), a.N, a.err));
       if (et == 0)
         ctl.seg_ok[buf] = mbar_wait_bounded(&ctl.tfull[buf], (it >> 1) & 1, a.wait_ns, abort_flag) ? 1 : 0;
       epi_bar();
@@ -1667,7 +1692,12 @@ size_t dn_slab_elems(int D, int nR) {
 cudaError_t launch_build_slabs(const uint16_t* Wp, const int* rc, int nC, int nR, int D, int N, const GuSlabGeom& g,
                                uint16_t* gu_slab, uint16_t* dn_slab, unsigned* err, cudaStream_t st) {
   if (gu_slab && g.P > 0) {
-    k_build_gu_slab<<<1184, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
+    const size_t chunks = gu_slab_elems(g) / 8;
+    const int grid = static_cast<int>(std::min<size_t>((chunks + 255) / 256, 152 * 16));
+    if (chunks < (size_t(1) << 31))
+      k_build_gu_slab<uint32_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
+    else
+      k_build_gu_slab<size_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

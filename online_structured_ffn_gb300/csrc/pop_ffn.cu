@@ -44,9 +44,13 @@ struct pop_ffn {
   int ldk = 0;
   int* ch_s = nullptr;     // channels of the selected candidates, in S order
   uint16_t* zcp = nullptr; // [N][2 * round_up(max_batch, 16)]: the candidates' z rows (hi, lo), B > 1
+  int* rcs = nullptr;      // skip variant: [C[S] | R], the list of the steps between updates
+  long long host_step = 0; // decode steps since the last partition (the device step counter's mirror)
   // B > 1 decode slabs (rebuilt at every partition): gate/up rows of R u C and down columns of R
   GuSlabGeom gu_geom{};
   uint16_t* gu_slab = nullptr;
+  GuSlabGeom gu_geom_skip{};          // skip variant: the gate/up slab of [C[S] | R], rebuilt at each
+  uint16_t* gu_slab_skip = nullptr;   // update step (B > 1)
   uint16_t* dn_slab = nullptr;
   int* step = nullptr;
   unsigned* err = nullptr;
@@ -126,7 +130,7 @@ void prof_end(pop_ffn* h) {
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
                   h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_s,
-                  h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab, h->zcp};
+                  h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab, h->zcp, h->rcs, h->gu_slab_skip};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -163,6 +167,15 @@ cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
   return cudaMemsetAsync(h->fsync, 0, kSyncWords * sizeof(unsigned), st);
 }
 
+// The skip variant's list [C[S] | R]: R after the k selected slots (stream-ordered after the
+// partition); the slots are written at each update step. Resets the host's step mirror.
+cudaError_t skip_list_tail(pop_ffn* h, cudaStream_t st) {
+  h->host_step = 0;
+  if (h->cnt.n_R == 0) return cudaSuccess;
+  return cudaMemcpyAsync(h->rcs + h->cnt.k, h->rc + h->cnt.n_C, sizeof(int) * h->cnt.n_R, cudaMemcpyDeviceToDevice,
+                         st);
+}
+
 // Rebuilds the B > 1 decode slabs from the current partition (stream-ordered after it).
 cudaError_t build_slabs(pop_ffn* h, cudaStream_t st) {
   if (!h->gu_slab) return cudaSuccess;
@@ -173,16 +186,16 @@ cudaError_t build_slabs(pop_ffn* h, cudaStream_t st) {
 // gate/up over the positions of rc = [C (nC) | R (nR)] for B tokens: z of the candidates (zc),
 // their scores, and the z planes of R.
 // The same from the gate/up slab of the current partition.
-pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st) {
+pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st, bool skip = false) {
   GateUpSlabArgs a{};
-  a.slab = h->gu_slab;
-  a.geom = h->gu_geom;
+  a.slab = skip ? h->gu_slab_skip : h->gu_slab;
+  a.geom = skip ? h->gu_geom_skip : h->gu_geom;
   a.D = h->D;
   a.N = h->N;
   a.B = B;
   a.NP = round_up(B, 16);
-  a.rc = h->rc;
-  a.nC = h->cnt.n_C;
+  a.rc = skip ? h->rcs : h->rc;
+  a.nC = skip ? h->cnt.k : h->cnt.n_C;
   a.nR = h->cnt.n_R;
   a.n2 = h->n2;
   a.zcp = h->zcp;
@@ -199,8 +212,10 @@ pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st) {
   return POP_OK;
 }
 
-pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st) {
+pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st,
+                     bool list_after_wait = false) {
   GateUpTcArgs a{};
+  a.list_after_wait = list_after_wait ? 1 : 0;
   a.Wp = h->Wp;
   a.D = h->D;
   a.N = h->N;
@@ -210,8 +225,7 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC
   a.nC = nC;
   a.nR = nR;
   a.n2 = h->n2;
-  a.zc = h->z;
-  a.ldzc = round_up(B, 4);
+  a.zcp = h->zcp;
   a.zk = h->zk;
   a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
   a.ldk = h->ldk;
@@ -228,7 +242,8 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC
 // The selection of this decode step (decode: when there are candidates) and y[b] = sum over the
 // kept items of z[b][item] W2[:, channel]: the nR items with channels ch_r[], then the k selected
 // candidates. decode = false: the dense path (no selection, no step count).
-pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decode, void* y, cudaStream_t st) {
+pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decode, void* y, cudaStream_t st,
+                   bool skip = false) {
   if (nR + k <= 0) {
     const size_t bytes = static_cast<size_t>(B) * h->D * (h->cfg.out_f32 ? 4 : 2);
     POP_CUDA(h, cudaMemsetAsync(y, 0, bytes, st));
@@ -254,7 +269,7 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.scores = h->scores;
   a.zcp = h->zcp;
   a.rc = h->rc;
-  a.nC = h->cnt.n_C;
+  a.nC = skip ? k : h->cnt.n_C;  // a skip step's candidates are the held selection
   a.period = h->cfg.period;
   a.memory = h->memory;
   a.S = h->S;
@@ -262,6 +277,13 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.count_step = decode ? 1 : 0;
   a.flag = h->fsync + 5;
   a.epoch = decode ? ++h->epoch : 0;
+  a.skip = skip ? 1 : 0;
+  a.S_hold = h->S;
+  a.rcs = h->cfg.skip && h->cfg.period > 1 ? h->rcs : nullptr;
+  if (skip) {
+    a.S = h->idx_all;  // the selected items are positions [0, k) of the skip list,
+    a.ch_s = h->rcs;   // and their channels its head (written by whichever path ran the update)
+  }
   a.err = h->err;
   a.wait_ns = h->wait_ns;
   POP_CUDA(h, launch_down_tc(a, h->num_sms, st));
@@ -328,6 +350,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
     return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: max_batch must be in [1, POP_MAX_BATCH]");
   if (cfg->max_prefill_tokens < 1)
     return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: max_prefill_tokens must be >= 1");
+  if (cfg->skip != 0 && cfg->skip != 1) return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: skip must be 0 or 1");
   if (!aligned16(Wg) || !aligned16(W1) || !aligned16(W2))
     return fail(nullptr, POP_ERR_INVALID_ARG, "pop_ffn_create: weights must be 16-byte aligned");
   pop_counts cnt;
@@ -381,6 +404,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->scores, N);
   POP_ALLOC(h->memory, N);
   POP_ALLOC(h->S, N);
+  POP_ALLOC(h->rcs, N);
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
   if (cfg->max_batch > 1) {
     POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
@@ -388,6 +412,10 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
     POP_ALLOC(h->zcp, static_cast<size_t>(N) * 2 * round_up(cfg->max_batch, 16));
     h->gu_geom = gu_slab_geom(cnt.n_C + cnt.n_R, D, h->num_sms);
     POP_ALLOC(h->gu_slab, gu_slab_elems(h->gu_geom));
+    if (cfg->skip && cfg->period > 1 && cnt.n_C > 0) {
+      h->gu_geom_skip = gu_slab_geom(cnt.k + cnt.n_R, D, h->num_sms);
+      POP_ALLOC(h->gu_slab_skip, gu_slab_elems(h->gu_geom_skip));
+    }
     POP_ALLOC(h->dn_slab, dn_slab_elems(D, cnt.n_R));
   }
   POP_ALLOC(h->step, 1);
@@ -407,6 +435,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   // index lists always hold valid positions, even before the first partition or selection
   if ((e = cudaMemsetAsync(h->S, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->rc, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
+  if ((e = cudaMemsetAsync(h->rcs, 0, sizeof(int) * N, st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   k_iota<<<(N + 255) / 256, 256, 0, st>>>(h->idx_all, N);
   if ((e = cudaGetLastError()) != cudaSuccess) return bail(e, "k_iota");
   if ((e = launch_pack(static_cast<const uint16_t*>(Wg), static_cast<const uint16_t*>(W1),
@@ -475,6 +504,7 @@ pop_status pop_prefill_partition(pop_ffn_t h, const void* X, int M, void* Y, voi
                                h->memory, h->err, st));
   POP_CUDA(h, reset_counters(h, st));
   POP_CUDA(h, build_slabs(h, st));
+  POP_CUDA(h, skip_list_tail(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -489,6 +519,7 @@ pop_status pop_partition_from_importance(pop_ffn_t h, const float* importance, v
                                h->err, st));
   POP_CUDA(h, reset_counters(h, st));
   POP_CUDA(h, build_slabs(h, st));
+  POP_CUDA(h, skip_list_tail(h, st));
   h->partitioned = true;
   h->selected = false;
   return POP_OK;
@@ -519,6 +550,7 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
   POP_CUDA(h, cudaMemsetAsync(h->memory, 0, sizeof(float) * (nC > 0 ? nC : 1), st));
   POP_CUDA(h, reset_counters(h, st));
   POP_CUDA(h, build_slabs(h, st));
+  POP_CUDA(h, skip_list_tail(h, st));
   POP_CUDA(h, cudaStreamSynchronize(st));
   h->partitioned = true;
   h->selected = false;
@@ -534,36 +566,57 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     return fail(h, POP_ERR_INVALID_ARG, "pop_decode_step: x, y must be 16-byte aligned");
   if (!h->partitioned) return fail(h, POP_ERR_STATE, "pop_decode_step: no partition (run a prefill first)");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int nC = h->cnt.n_C, nR = h->cnt.n_R;
+  const int nC = h->cnt.n_C, nR = h->cnt.n_R, k = h->cnt.k;
+  // skip variant: steps between updates run over R and the held selection only (the device step
+  // counter advances with every step, so the host's mirror tells the update steps apart)
+  const bool skip_mode = h->cfg.skip && h->cfg.period > 1 && nC > 0;
+  const bool skip = skip_mode && (h->host_step % h->cfg.period) != 0;
+  int* rcs = skip_mode ? h->rcs : nullptr;
   prof_begin(h);
   if (B == 1) {
     const int grid = h->num_sms * 4;
-    DecodeB1Args a = b1_args(h, static_cast<const uint16_t*>(x), y, h->rc, nC, nR);
-    a.do_select = nC <= FZ_MAX_C ? 1 : 0;
-    a.k = h->cnt.k;
-    a.kd = h->cnt.k;
+    DecodeB1Args a = skip ? b1_args(h, static_cast<const uint16_t*>(x), y, h->rcs, k, nR)
+                          : b1_args(h, static_cast<const uint16_t*>(x), y, h->rc, nC, nR);
+    a.do_select = skip || nC <= FZ_MAX_C ? 1 : 0;
+    a.skip = skip ? 1 : 0;
+    a.S_hold = h->S;
+    a.rcs = rcs;
+    a.k = k;
+    a.kd = k;
+    if (skip) a.S = h->idx_all;  // the down projection's selected items: positions [0, k) of the list
     prof_mark(h, 0, st);
     POP_CUDA(h, launch_gateup_sel_b1(a, grid, st));
     prof_mark(h, 1, st);
     if (!a.do_select)
-      POP_CUDA(h, launch_select(h->scores, h->memory, nC, h->cnt.k, h->cfg.period, h->step, h->S, h->err, st));
+      POP_CUDA(h, launch_select(h->scores, h->memory, nC, k, h->cfg.period, h->step, h->S, h->rc, rcs, h->err, st));
     prof_mark(h, 2, st);
     POP_CUDA(h, launch_down_tiled_b1(a, h->num_sms, st));
     prof_mark(h, 3, st);
+    // skip variant, update step: a later B > 1 skip step streams the slab of this selection's list
+    if (skip_mode && !skip && h->gu_slab_skip)
+      POP_CUDA(h, launch_build_slabs(h->Wp, h->rcs, k, nR, h->D, h->N, h->gu_geom_skip, h->gu_slab_skip, nullptr,
+                                     h->err, st));
     prof_mark(h, 4, st);
   } else {
-    // gate/up, then the down GEMM over R and the selected items with the selection inside
+    // gate/up, then the down GEMM over R and the selected items with the selection inside; a skip
+    // step gathers the rows of R and of the held selection instead of streaming the slab
     prof_mark(h, 0, st);
-    pop_status s = gateup_slab(h, static_cast<const uint16_t*>(x), B, st);
+    pop_status s = gateup_slab(h, static_cast<const uint16_t*>(x), B, st, skip);
     if (s != POP_OK) return s;
     prof_mark(h, 1, st);
     prof_mark(h, 2, st);
-    s = down_tc(h, B, h->rc + nC, nR, h->cnt.k, true, y, st);
+    s = down_tc(h, B, h->rc + nC, nR, k, true, y, st, skip);
     if (s != POP_OK) return s;
     prof_mark(h, 3, st);
+    // skip variant, update step: the slab of [C[S] | R] for the steps until the next update (an
+    // ordinary launch: it starts once the selection's list is complete)
+    if (skip_mode && !skip && h->gu_slab_skip)
+      POP_CUDA(h, launch_build_slabs(h->Wp, h->rcs, k, nR, h->D, h->N, h->gu_geom_skip, h->gu_slab_skip, nullptr,
+                                     h->err, st));
     prof_mark(h, 4, st);
   }
   prof_end(h);
+  ++h->host_step;
   h->selected = true;
   return POP_OK;
 }

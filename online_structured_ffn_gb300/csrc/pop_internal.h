@@ -37,8 +37,10 @@ struct GateUpTcArgs {
   const int* rc;         // position -> channel: [C | R]
   int nC, nR;
   const float* n2;       // ||W2[:, c]||
-  float* zc;             // out: z of the candidate positions, fp32 [nC][ldzc] (tokens contiguous)
-  int ldzc;              // round_up(B, 4)
+  uint16_t* zcp;         // out: z of the candidate positions as rows of 2 NP bf16 (hi parts of the
+                         // tokens, then lo parts), [nC][2 NP]
+  int list_after_wait;   // 1: rc may have been written by the previous kernel (a skip step's list):
+                         //    every producer waits for it before reading rc
   uint16_t* zk;          // out: z of R as bf16 hi parts at [b][p - nC] (row stride ldk)
   uint16_t* zk_lo;       // ... and bf16 lo parts z - hi
   int ldk;
@@ -75,6 +77,10 @@ struct DownTcArgs {
   int count_step;        // 1: advance the step counter (decode)
   unsigned* flag;        // selection of step `epoch` complete when *flag == epoch
   unsigned epoch;
+  int skip;              // a skip-variant step between updates: the selecting CTA adds the scores of
+                         // positions [0, k) to the memory at S_hold and selects nothing; S is [0, k)
+  const int* S_hold;
+  int* rcs;              // skip variant, update steps: rcs[j] = channel of selected j (or NULL)
   // work split (set by the launcher)
   int split, units;
   unsigned* err;
@@ -132,6 +138,10 @@ struct DecodeB1Args {
   const int* rc;       // [C | R] channel indices (or all channels for the dense path)
   int nC, nR;
   int do_select;       // 1: CTA 0 of the gate/up grid runs the memory update and the top-k
+  int skip;            // 1: a step between updates of the skip variant: rc lists [C[S] | R], nC = k,
+                       //    CTA 0 adds the scores to the memory at the held positions S_hold
+  const int* S_hold;   // the held selection (positions into C) on skip steps
+  int* rcs;            // skip variant, update steps: CTA 0 writes rcs[j] = rc[S[j]] (or NULL)
   int k;               // candidates to select
   int kd;              // selected candidates the down projection adds (k, or 0 for the dense path)
   int period;
@@ -162,8 +172,9 @@ constexpr int FZ_MAX_C = 8192;
 cudaError_t launch_partition(const float* sumsq, const float* n2, float* I, int N, int n_P, int n_R, int* rc,
                              int* P, int* step, float* memory, unsigned* err, cudaStream_t st);
 // Candidate selection for one decode step (periodic memory, top-k, step counter).
+// rcs (skip variant, or NULL): on update steps rcs[j] = rc[S[j]] for the selected j < k
 cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
-                          unsigned* err, cudaStream_t st);
+                          const int* rc, int* rcs, unsigned* err, cudaStream_t st);
 // sumsq[i] (+)= sum over rows p < rows of part[p * ld + i], p ascending.
 cudaError_t launch_fold_sumsq(const float* part, int rows, int ld, int N, float* sumsq, int accumulate,
                               cudaStream_t st);

@@ -81,15 +81,25 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 // ------------------------------------------------------------------ per-step candidate selection
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     k_select(const float* __restrict__ scores, float* __restrict__ memory, int nC, int k, int period,
-             int* __restrict__ step, int* __restrict__ S, unsigned* __restrict__ err) {
+             int* __restrict__ step, int* __restrict__ S, const int* __restrict__ rc, int* __restrict__ rcs,
+             unsigned* __restrict__ err) {
   extern __shared__ uint32_t keys[];
   __shared__ RadixScratch<SEL_THREADS> sc;
   const int t = *step;
+  const bool update = (t % period) == 0;
   const bool ok = select_step<SEL_THREADS>(
-      threadIdx.x, [&](int i) { return scores[i]; }, memory, nC, k, period, (t % period) == 0, keys, S, sc,
-      BlockSync());
+      threadIdx.x, [&](int i) { return scores[i]; }, memory, nC, k, period, update, keys, S, sc, BlockSync());
   if (!ok && threadIdx.x == 0) atomicOr(err, DEVERR_TOPK);
   __syncthreads();
+  if (rcs && update)  // skip variant: the selected channels head the list of the steps until the next update
+    for (int j = threadIdx.x; j < k; j += SEL_THREADS) {
+      int ps = S[j];
+      if (static_cast<unsigned>(ps) >= static_cast<unsigned>(nC)) {
+        atomicOr(err, DEVERR_INDEX);
+        ps = 0;
+      }
+      rcs[j] = rc[ps];
+    }
   if (threadIdx.x == 0) *step = t + 1;
 }
 
@@ -114,13 +124,16 @@ cudaError_t launch_partition(const float* sumsq, const float* n2, float* I, int 
 }
 
 cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int period, int* step, int* S,
-                          unsigned* err, cudaStream_t st) {
+                          const int* rc, int* rcs, unsigned* err, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(nC > 0 ? nC : 1) * sizeof(uint32_t);
-  if (smem > 48 * 1024) {
+  // the keys plus the kernel's static scratch can pass the 48 KB default even below 48 KB of keys
+  static size_t configured = 0;
+  if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    configured = smem;
   }
-  k_select<<<1, SEL_THREADS, smem, st>>>(scores, memory, nC, k, period, step, S, err);
+  k_select<<<1, SEL_THREADS, smem, st>>>(scores, memory, nC, k, period, step, S, rc, rcs, err);
   return cudaGetLastError();
 }
 

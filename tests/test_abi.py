@@ -64,7 +64,8 @@ def test_create_rejects_bad_config_before_touching_cuda(pop):
     good = dict(D=256, D_FF=1024, r=0.3, gamma=0.1, period=1, max_batch=1, max_prefill_tokens=64, out_f32=1)
     fake = 4096  # any 16-byte aligned non-null value: the checks below fail before it is used
     bad = [dict(D=100), dict(D=0), dict(D=20000), dict(D_FF=0), dict(D_FF=60000), dict(period=0),
-           dict(max_batch=0), dict(max_batch=65), dict(max_prefill_tokens=0), dict(r=1.5), dict(gamma=-1.0)]
+           dict(max_batch=0), dict(max_batch=65), dict(max_prefill_tokens=0), dict(r=1.5), dict(gamma=-1.0),
+           dict(skip=2), dict(skip=-1)]
     for b in bad:
         cfg = pop.pop_config(**{**good, **b})
         assert lib.pop_ffn_create(ctypes.byref(cfg), fake, fake, fake, None, ctypes.byref(out)) == \

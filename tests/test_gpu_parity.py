@@ -240,6 +240,68 @@ def test_periodic_memory(env, period, B):
     lay.close()
 
 
+@pytest.mark.parametrize("D,N,r,period,B", [(256, 1024, 0.5, 4, 1), (512, 2048, 0.3, 4, 16), (256, 1024, 0.5, 3, 33),
+                                             (64, 46000, 0.3, 4, 1), (256, 2048, 0.5, 16, 64)])
+def test_periodic_skip_variant(env, D, N, r, period, B):
+    """Between updates gate/up runs over R and the held selection only; the memory gains the
+    held selection's scores; update steps select from it (the oracle's skip reading)."""
+    lay = Layer(env, D, N, r=r, gamma=0.1, period=period, max_batch=B, skip=True)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 32, lay.sc)), r, 0.1)
+    lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k, period=period, skip=True)
+    held = None
+    diverged = False
+    for t in range(2 * period + 2):
+        x = synth.decode_input(0, t, B, lay.sc)
+        y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+        mem_before = sess.memory.copy()
+        y_ref = sess.step(f64(x))
+        S = lay.ffn.selected()
+        if t % period == 0:
+            if not diverged:
+                used = mem_before + sess.last_scores
+                bad, _, nd = parity.compare_selection(S, sess.C[sess.S], sess.C, used, lay.counts.k)
+                assert not bad, f"step {t}: selection differs outside the flagged band"
+                diverged = nd > 0  # a flagged near-tie flipped: the sessions hold different sets from here
+            held = S.copy()
+        else:
+            assert np.array_equal(S, held), "selection must be held between updates"
+        if not diverged:
+            parity.check_y(y, y_ref, f"skip step {t}")
+            _, mem = lay.ffn.scores()
+            amax = max(np.abs(sess.memory).max(), 1e-30)
+            assert np.all(np.abs(mem - sess.memory) <= 1e-4 * np.abs(sess.memory) + 1e-5 * amax), f"memory, step {t}"
+    assert lay.ffn.step_count() == 2 * period + 2
+    lay.ffn.check()
+    lay.close()
+
+
+def test_periodic_skip_mixed_batch_sizes(env):
+    """Update and skip steps at B = 1 and B > 1 interleaved on one handle (the skip steps' slab is
+    rebuilt by whichever path ran the update)."""
+    D, N, r, period = 256, 1024, 0.5, 3
+    lay = Layer(env, D, N, r=r, gamma=0.1, period=period, max_batch=8, skip=True)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 32, lay.sc)), r, 0.1)
+    lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k, period=period, skip=True)
+    for t, B in enumerate([1, 8, 8, 8, 1, 1, 1, 8, 2]):
+        x = synth.decode_input(0, t, B, lay.sc)
+        y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+        mem_before = sess.memory.copy()
+        y_ref = sess.step(f64(x))
+        if t % period == 0:
+            bad, _, nd = parity.compare_selection(lay.ffn.selected(), sess.C[sess.S], sess.C,
+                                                  mem_before + sess.last_scores, lay.counts.k)
+            assert not bad
+            if nd:
+                break  # a flagged near-tie flipped: the sessions hold different sets from here
+        parity.check_y(y, y_ref, f"mixed skip step {t} (B={B})")
+    lay.ffn.check()
+    lay.close()
+
+
 def test_period_one_equals_per_step(env):
     D, N = 256, 1024
     a = Layer(env, D, N, r=0.5, gamma=0.1, period=1)
