@@ -26,8 +26,8 @@
 // the landed copies for the tensor cores after its barrier wait.
 //
 // Gate/up by gathering (k_gateup_tc, used by the dense reference path at B > 1, where every
-// channel is kept and no slab exists): one CTA per SM; each CTA streams "units" of at most 64 positions over all
-// of K. The unit ranges are ragged (P / units each) so that the number of units matches the number
+// channel is kept and no slab exists): one CTA per SM; each CTA streams "units" of at most 64
+// positions over all of K. The unit ranges are ragged (P / units each) so that the number of units matches the number
 // of CTAs. One MMA covers gate and up of a unit together: TMEM lane quarter q holds gate rows
 // 16q..16q+15 in lanes 0-15 and the up rows of the same positions in lanes 16-31, so an epilogue
 // warp pairs them with one shuffle. Rows past a unit's end are never written and the accumulator
@@ -393,7 +393,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int u = 0; u < KS; ++u)
         tma_load_2d(smem + s * STAGE + u * SUB + AROWS * 128, &mapX, &ctl.full[s], (sbk * KS + u) * TC_BK, 0);
     };
-    if (a.list_after_wait) pdl_wait();  // the list itself is this step's data
     for (int u = w; u < U && ok; u += W) {
       const int lo = unit_lo(u), nrows = unit_lo(u + 1) - lo;
       uint32_t rowbase[4], dst[4];
@@ -404,7 +403,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         dst[t] = 0u;
         if (rr < 2 * nrows) {
           const int g = rr & 1, j = rr >> 1;
-          const int ch = guard_ch(a.list_after_wait ? __ldcg(a.rc + lo + j) : __ldg(a.rc + lo + j), a.N, a.err);
+          const int ch = guard_ch(__ldg(a.rc + lo + j), a.N, a.err);
           const int arow = 32 * (j >> 4) + 16 * g + (j & 15);
           rowbase[t] = static_cast<uint32_t>(ch) * row3 + static_cast<uint32_t>(g) * a.D + 8 * cq;
           dst[t] = arow * 128 + ((cq ^ (arow & 7)) << 4);
@@ -1671,6 +1670,10 @@ GuSlabGeom gu_slab_geom(int P, int D, int num_sms) {
   if (T < W) T = P > 0 ? (W < (P + 15) / 16 ? W : (P + 15) / 16) : 1;
   g.T = T > 0 ? T : 1;
   g.RT = P > 0 ? (P + g.T - 1) / g.T : 1;
+  // whole row groups: a paired tile stores gate and up of 16 positions per 32 rows, an unpaired
+  // one 8-row blocks, so other tile sizes leave rows that are streamed but hold nothing (44
+  // positions in 96 rows, 10% of the bytes); fewer, fuller tiles stream fewer bytes in all
+  g.RT = g.RT <= GU_MAX_ROWS ? (g.RT + 15) / 16 * 16 : (g.RT + 7) / 8 * 8;
   g.T = P > 0 ? (P + g.RT - 1) / g.RT : 1;
   g.paired = g.RT <= GU_MAX_ROWS ? 1 : 0;
   if (g.paired) {

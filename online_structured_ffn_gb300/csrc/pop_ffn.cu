@@ -212,10 +212,8 @@ pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st, bo
   return POP_OK;
 }
 
-pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st,
-                     bool list_after_wait = false) {
+pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC, int nR, cudaStream_t st) {
   GateUpTcArgs a{};
-  a.list_after_wait = list_after_wait ? 1 : 0;
   a.Wp = h->Wp;
   a.D = h->D;
   a.N = h->N;

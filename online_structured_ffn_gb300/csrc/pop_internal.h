@@ -39,8 +39,6 @@ struct GateUpTcArgs {
   const float* n2;       // ||W2[:, c]||
   uint16_t* zcp;         // out: z of the candidate positions as rows of 2 NP bf16 (hi parts of the
                          // tokens, then lo parts), [nC][2 NP]
-  int list_after_wait;   // 1: rc may have been written by the previous kernel (a skip step's list):
-                         //    every producer waits for it before reading rc
   uint16_t* zk;          // out: z of R as bf16 hi parts at [b][p - nC] (row stride ldk)
   uint16_t* zk_lo;       // ... and bf16 lo parts z - hi
   int ldk;

@@ -75,7 +75,6 @@ def _decode(env, ffn, W, sc, r, gamma, B, steps, period=1, prompt_len=8, skip=Fa
     ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, prompt_len, sc)), r, gamma)
     ffn.set_partition(ref["R"], ref["C"], ref["P"])
     sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], ref["counts"].k, period=period, skip=skip)
-    checked = 0
     held_differs = False  # a flagged near-tie flipped at an update: the held sets differ until the next
     for t in range(steps):
         x = synth.decode_input(0, t, B, sc)
@@ -88,11 +87,13 @@ def _decode(env, ffn, W, sc, r, gamma, B, steps, period=1, prompt_len=8, skip=Fa
             assert not bad, f"step {t}: selection differs outside the flagged band"
             held_differs = nd > 0
         if held_differs:
-            continue
+            # the GPU holds another valid set (a flagged near-tie went the other way): its y must be
+            # the FFN over R and that set
+            keep = np.sort(np.concatenate([ref["R"], ffn.selected()]))
+            Z = oracle.ffn_activations(Wg[keep], W1[keep], f64(x))
+            y_ref = Z @ W2[:, keep].T
         parity.check_y(y, y_ref, f"B={B} step {t}")
-        checked += 1
     ffn.check()
-    assert checked >= 1
 
 
 @pytest.mark.parametrize("B,r", [(1, 0.299), (16, 0.5)])
