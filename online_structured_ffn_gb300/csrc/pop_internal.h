@@ -160,7 +160,10 @@ int down_tiled_chunks(int D, int nitems, int num_sms);
 cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st);
 cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st);
 
-// largest |C| whose top-k runs inside the B = 1 gate/up kernel (its keys sit in shared memory)
+// largest |C| whose top-k runs inside the B = 1 gate/up kernel (its keys sit in shared memory).
+// Larger candidate sets are selected by a kernel of their own: when (nearly) every channel is a
+// candidate the in-kernel top-k cannot overlap the R stream, and measured slower than the
+// separate kernel (full re-evaluation at D_FF = 11008: step 66 us against 58 us).
 constexpr int FZ_MAX_C = 8192;
 
 // ---- selection (pop_select.cu)

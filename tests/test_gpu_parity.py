@@ -159,10 +159,11 @@ def test_decode_parity_shapes(env, D, N):
 @pytest.mark.parametrize("D,N,r,gamma,period", [(512, 2048, 0.3, 0.1, 1), (4096, 11008, 0.299, 0.1, 1),
                                                 (256, 1024, 0.5, 0.1, 4), (1024, 600, 0.3, 0.0, 1),
                                                 (1024, 600, 0.4, 0.6, 1), (2048, 333, 0.0, 0.1, 1),
+                                                (256, 8192, 0.4, 0.6, 1), (256, 8193, 0.4, 0.6, 1),
                                                 (256, 20000, 0.4, 0.6, 1), (256, 20000, 0.5, 0.5, 3)])
 def test_single_token_paths(env, D, N, r, gamma, period):
     # B = 1: the top-k runs inside the gate/up kernel for |C| <= 8192 and as its own kernel above
-    # (the last two shapes have |C| = 20000).
+    # (|C| = 8192 and 8193 on either side of the limit, then 20000).
     lay = Layer(env, D, N, r=r, gamma=gamma, period=period)
     Wg, W1, W2 = lay.w64()
     ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 8, lay.sc)), r, gamma)
@@ -240,14 +241,17 @@ def test_periodic_memory(env, period, B):
     lay.close()
 
 
-@pytest.mark.parametrize("D,N,r,period,B", [(256, 1024, 0.5, 4, 1), (512, 2048, 0.3, 4, 16), (256, 1024, 0.5, 3, 33),
-                                             (64, 46000, 0.3, 4, 1), (256, 2048, 0.5, 16, 64)])
-def test_periodic_skip_variant(env, D, N, r, period, B):
+@pytest.mark.parametrize("D,N,r,gamma,period,B", [(256, 1024, 0.5, 0.1, 4, 1), (512, 2048, 0.3, 0.1, 4, 16),
+                                                   (256, 1024, 0.5, 0.1, 3, 33), (64, 48000, 0.3, 0.15, 4, 1),
+                                                   (256, 2048, 0.5, 0.1, 16, 64)])
+def test_periodic_skip_variant(env, D, N, r, gamma, period, B):
     """Between updates gate/up runs over R and the held selection only; the memory gains the
-    held selection's scores; update steps select from it (the oracle's skip reading)."""
-    lay = Layer(env, D, N, r=r, gamma=0.1, period=period, max_batch=B, skip=True)
+    held selection's scores; update steps select from it (the oracle's skip reading). The 48000
+    channel case has |C| = 14400, above the in-kernel top-k's limit at B = 1 (the separate top-k
+    kernel writes the list)."""
+    lay = Layer(env, D, N, r=r, gamma=gamma, period=period, max_batch=B, skip=True)
     Wg, W1, W2 = lay.w64()
-    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 32, lay.sc)), r, 0.1)
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 32, lay.sc)), r, gamma)
     lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
     sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k, period=period, skip=True)
     held = None
