@@ -404,12 +404,9 @@ cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t s
   const size_t smem = keys > xsz ? keys : xsz;
 #define POP_GS(NC)                                                                                              \
   case NC: {                                                                                                    \
-    static size_t configured = 0;                                                                               \
-    if (smem > configured) {  /* the static scratch counts toward the 48 KB default too */                    \
-      cudaError_t e = cudaFuncSetAttribute(k_gateup_sel_b1<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                           static_cast<int>(smem));                                             \
+    {                                                                                                           \
+      cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(k_gateup_sel_b1<NC>), smem);                \
       if (e != cudaSuccess) return e;                                                                           \
-      configured = smem;                                                                                        \
     }                                                                                                           \
     { cudaError_t e = launch_pdl(k_gateup_sel_b1<NC>, dim3(grid), dim3(GS_THREADS), smem, st, a);             \
       if (e != cudaSuccess) return e; }                                                                         \

@@ -56,6 +56,7 @@
 // returns. The warps of a role take every decision that guards a named barrier together, and every
 // thread reaches the cluster barriers, so a time-out cannot leave a barrier waiting.
 #include <algorithm>
+#include <mutex>
 
 #include "pop_device.cuh"
 #include "pop_internal.h"
@@ -1503,12 +1504,9 @@ cudaError_t launch_gateup_np(const CUtensorMap& xm, GateUpTcArgs a, int num_sms,
   const int P = a.nC + a.nR;
   if (P <= 0) return cudaSuccess;
   const GuSplit g = gateup_split(P, NP, num_sms);
-  static size_t configured = 0;
-  if (g.smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gateup_tc<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(g.smem));
+  {
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(k_gateup_tc<NP>), g.smem);
     if (e != cudaSuccess) return e;
-    configured = g.smem;
   }
   a.units = g.units;
   a.rows_cap = g.rows_cap;
@@ -1548,12 +1546,9 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
     const size_t want = small_bytes <= kMaxDyn ? small_bytes : keys_bytes;
     if (want > smem) smem = want;
   }
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_down_tc<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  {
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(k_down_tc<NP>), smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   const int G = a.D / 8;
   const int tiles = (a.D + TC_BM - 1) / TC_BM;
@@ -1589,6 +1584,8 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
   };
   static Entry cache[8];
   static int cache_n = 0;
+  static std::mutex cache_mu;
+  std::lock_guard<std::mutex> lock(cache_mu);
   int dev = 0;
   (void)cudaGetDevice(&dev);
   const int slab = a.dslab != nullptr ? 1 : 0;
@@ -1741,15 +1738,10 @@ cudaError_t launch_gateup_slab_np(const CUtensorMap& xm, GateUpSlabArgs a, int n
   stages = stages > TC_MAX_STAGES ? TC_MAX_STAGES : stages;
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = 1024 + static_cast<size_t>(stages) * stage + slack;
-  static size_t configured[2] = {0, 0};
-  const int pi = g.paired ? 1 : 0;
-  if (smem > configured[pi]) {
-    cudaError_t e = g.paired ? cudaFuncSetAttribute(k_gateup_slab<NP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    static_cast<int>(smem))
-                             : cudaFuncSetAttribute(k_gateup_slab<NP, false>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  {
+    cudaError_t e = g.paired ? ensure_dyn_smem(reinterpret_cast<const void*>(k_gateup_slab<NP, true>), smem)
+                             : ensure_dyn_smem(reinterpret_cast<const void*>(k_gateup_slab<NP, false>), smem);
     if (e != cudaSuccess) return e;
-    configured[pi] = smem;
   }
   a.ks = ks;
   a.stages = stages;

@@ -5,6 +5,9 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "pop_ffn.h"
@@ -295,6 +298,20 @@ __global__ void k_iota(int* a, int n) {
 }  // namespace
 
 void pop::set_unbound_error(const char* msg) { g_msg = msg; }
+
+cudaError_t pop::ensure_dyn_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> configured;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = configured[{kernel, dev}];
+  if (bytes <= have) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 extern "C" {
 

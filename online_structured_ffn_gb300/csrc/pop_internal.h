@@ -160,6 +160,11 @@ int down_tiled_chunks(int D, int nitems, int num_sms);
 cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st);
 cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st);
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per kernel,
+// device and size (the attribute is per device; thread-safe). Call before every launch that needs
+// more than the 48 KB default, counting the kernel's static shared memory in.
+cudaError_t ensure_dyn_smem(const void* kernel, size_t bytes);
+
 // largest |C| whose top-k runs inside the B = 1 gate/up kernel (its keys sit in shared memory).
 // Larger candidate sets are selected by a kernel of their own: when (nearly) every channel is a
 // candidate the in-kernel top-k cannot overlap the R stream, and measured slower than the

@@ -127,11 +127,9 @@ cudaError_t launch_select(const float* scores, float* memory, int nC, int k, int
                           const int* rc, int* rcs, unsigned* err, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(nC > 0 ? nC : 1) * sizeof(uint32_t);
   // the keys plus the kernel's static scratch can pass the 48 KB default even below 48 KB of keys
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  {
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(k_select), smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   k_select<<<1, SEL_THREADS, smem, st>>>(scores, memory, nC, k, period, step, S, rc, rcs, err);
   return cudaGetLastError();

@@ -142,8 +142,7 @@ pop_status pop_ffn_dense_token_noalloc(const void* Wg, const void* W1, const voi
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t smem = static_cast<size_t>(D) * sizeof(float);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(k_static_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (pop::ensure_dyn_smem(reinterpret_cast<const void*>(k_static_gateup), smem) != cudaSuccess)
     return static_fail(POP_ERR_CUDA, "dense_token_noalloc: cudaFuncSetAttribute failed");
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
