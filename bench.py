@@ -231,9 +231,17 @@ class Stack:
         # B > 1 the two slab builders); decode at B = 1: gate/up with the top-k inside (+ a separate
         # top-k when |C| > 8192) and the tiled down projection; at B > 1: the gate/up GEMM, then the
         # down GEMM with the selection inside
-        per_layer = prefill_launches(self.chunks, self.wl["B"]) + decode_launches(self.counts, self.wl["B"]) * \
-            self.wl["T"]
-        return per_layer * self.wl["layers"]
+        wl, c = self.wl, self.counts
+        T, B = wl["T"], wl["B"]
+        decode = decode_launches(c, B) * T
+        if wl.get("skip") and wl["period"] > 1 and c.n_C > 0:
+            updates = (T + wl["period"] - 1) // wl["period"]
+            if B > 1:
+                decode += updates  # the slab of [C[S] | R] rebuilt after each update
+            elif c.n_C > 8192:
+                decode -= T - updates  # steps between updates need no separate top-k
+        per_layer = prefill_launches(self.chunks, B) + decode
+        return per_layer * wl["layers"]
 
     def session(self, dec_events=None):
         pop, torch = self.pop, self.torch

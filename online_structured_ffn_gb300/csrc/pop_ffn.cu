@@ -752,6 +752,10 @@ pop_status pop_check(pop_ffn_t h) {
   POP_CUDA(h, cudaMemset(h->err, 0, sizeof(unsigned)));
   POP_CUDA(h, reset_counters(h, nullptr));
   POP_CUDA(h, cudaDeviceSynchronize());
+  // a step that gave up may not have counted itself: the host's mirror follows the device counter
+  int dstep = 0;
+  POP_CUDA(h, cudaMemcpy(&dstep, h->step, sizeof(int), cudaMemcpyDeviceToHost));
+  h->host_step = dstep;
   char buf[240];
   std::snprintf(buf, sizeof buf,
                 "device error word 0x%x (1/2/32/64: prefill gate-up / prefill down / decode selector / decode "

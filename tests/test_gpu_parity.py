@@ -388,6 +388,39 @@ def test_bf16_output(env):
     lay.close()
 
 
+def test_bounded_wait_runs_out_and_the_handle_stays_usable(env):
+    """The B = 1 selector waits (bounded) for every candidate's score. With a 200 ns limit that
+    wait runs out: the kernel records a time-out in the device error word and returns, pop_check
+    reports POP_ERR_TIMEOUT and clears it, and with the limit restored the next steps match the
+    oracle (the step that timed out selected nothing and left the step count and memory alone)."""
+    pop, torch, dev = env
+    D, N, r = 4096, 11008, 0.299
+    lay = Layer(env, D, N, r=r, gamma=0.1, max_batch=1)
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 8, lay.sc)), r, 0.1)
+    lay.ffn.set_partition(ref["R"], ref["C"], ref["P"])
+    lay.ffn.set_wait_limit(200)
+    lay.ffn.decode_step(up(env, synth.decode_input(0, 99, 1, lay.sc)))
+    with pytest.raises(pop.PopError) as e:
+        lay.ffn.check()
+    assert e.value.status == pop.POP_ERR_TIMEOUT
+    lay.ffn.check()  # cleared
+    assert lay.ffn.step_count() == 0
+    lay.ffn.set_wait_limit(2_000_000_000)
+    sess = oracle.PopSession(Wg, W1, W2, ref["R"], ref["C"], lay.counts.k)
+    for t in range(2):
+        x = synth.decode_input(0, t, 1, lay.sc)
+        y = lay.ffn.decode_step(up(env, x)).cpu().numpy()
+        y_ref = sess.step(f64(x))
+        bad, _, nd = parity.compare_selection(lay.ffn.selected(), sess.C[sess.S], sess.C, sess.last_scores,
+                                              lay.counts.k)
+        assert not bad
+        if nd == 0:
+            parity.check_y(y, y_ref, f"step {t} after the time-out")
+    lay.ffn.check()
+    lay.close()
+
+
 def test_state_and_argument_errors(env):
     pop, torch, dev = env
     lay = Layer(env, 256, 1024, r=0.3, gamma=0.1, max_batch=2)
