@@ -615,8 +615,11 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* src, uint32
 // IDX is the index type: 32-bit when the chunk count allows it (64-bit division is slow here).
 template <class IDX>
 __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __restrict__ rc, int D, int N,
-                                GuSlabGeom g, uint16_t* __restrict__ slab, unsigned* __restrict__ err) {
-  const IDX total = static_cast<IDX>(g.T) * g.KB * g.arows * 8;
+                                GuSlabGeom g, int t_lo, int t_hi, uint16_t* __restrict__ slab,
+                                unsigned* __restrict__ err) {
+  // chunks of tiles [t_lo, t_hi); chunk e of this range is chunk e0 + e of the slab
+  const IDX e0 = static_cast<IDX>(t_lo) * g.KB * g.arows * 8;
+  const IDX total = static_cast<IDX>(t_hi - t_lo) * g.KB * g.arows * 8;
   const int grows = (g.RT + 7) / 8 * 8;
   const IDX arows = static_cast<IDX>(g.arows), KB = static_cast<IDX>(g.KB);
   for (IDX e = static_cast<IDX>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
@@ -626,7 +629,7 @@ __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __re
     const int ar = static_cast<int>(rest % arows);
     rest /= arows;
     const int kb = static_cast<int>(rest % KB);
-    const int t = static_cast<int>(rest / KB);
+    const int t = t_lo + static_cast<int>(rest / KB);
     const int c = pos ^ (ar & 7);
     int j, gu;
     if (g.paired) {
@@ -637,10 +640,10 @@ __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __re
       gu = ar >= grows ? 1 : 0;
       j = gu ? ar - grows : ar;
     }
-    const int p = t * g.RT + j;
+    const int p = gu_slab_pos(g, t, j);
     const int d = kb * TC_BK + 8 * c;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (j < g.RT && p < g.P && d < D) {
+    if (p >= 0 && d < D) {
       int ch = __ldcg(rc + p);
       if (static_cast<unsigned>(ch) >= static_cast<unsigned>(N)) {
         atomicOr(err, DEVERR_INDEX);
@@ -648,7 +651,7 @@ __global__ void k_build_gu_slab(const uint16_t* __restrict__ Wp, const int* __re
       }
       v = ldg_stream(Wp + static_cast<size_t>(ch) * 3 * D + static_cast<size_t>(gu) * D + d);
     }
-    *reinterpret_cast<uint4*>(slab + static_cast<size_t>(e) * 8) = v;
+    *reinterpret_cast<uint4*>(slab + static_cast<size_t>(e0 + e) * 8) = v;
   }
 }
 
@@ -876,8 +879,8 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
       // halves between them); unpaired: lane l holds gate (columns [0, NP)) and up ([NP, 2 NP)) of
       // position 32 q + l
       const int j = PAIRED ? 16 * q + (lane & 15) : 32 * q + lane;
-      const int p = t * g.RT + j;
-      const bool valid = j < g.RT && p < g.P;
+      const int p = gu_slab_pos(g, t, j);
+      const bool valid = p >= 0;
       const bool cand = valid && p < a.nC;
       const int half = PAIRED ? (lane >> 4) : 0;
       float n2v = 0.f;
@@ -1657,6 +1660,41 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
 }
 }  // namespace
 
+cudaError_t launch_build_gu_tiles(const uint16_t* Wp, const int* rc, int D, int N, const GuSlabGeom& g, int t_lo,
+                                  int t_hi, uint16_t* gu_slab, unsigned* err, cudaStream_t st) {
+  if (!gu_slab || g.P <= 0 || t_hi <= t_lo) return cudaSuccess;
+  const size_t chunks = static_cast<size_t>(t_hi - t_lo) * g.KB * g.arows * 8;
+  const int grid = static_cast<int>(std::min<size_t>((chunks + 255) / 256, 152 * 16));
+  if (gu_slab_elems(g) / 8 < (size_t(1) << 31))
+    k_build_gu_slab<uint32_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, t_lo, t_hi, gu_slab, err);
+  else
+    k_build_gu_slab<size_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, t_lo, t_hi, gu_slab, err);
+  return cudaGetLastError();
+}
+
+GuSlabGeom gu_slab_geom_split(int P1, int P, int D, int num_sms) {
+  GuSlabGeom g = gu_slab_geom(P, D, num_sms);
+  if (P1 <= 0 || P1 >= P) return g;
+  const int W = num_sms > 0 ? num_sms : 1;
+  // the same tile size, each region rounded up to whole tiles; grow the tiles while the two
+  // regions need more tiles than there are SMs
+  for (;;) {
+    g.Ts = (P1 + g.RT - 1) / g.RT;
+    g.T = g.Ts + (P - P1 + g.RT - 1) / g.RT;
+    if (g.T <= W) break;
+    g.RT += g.RT < GU_MAX_ROWS ? 16 : 8;
+  }
+  g.P1 = P1;
+  g.paired = g.RT <= GU_MAX_ROWS ? 1 : 0;
+  if (g.paired) {
+    const int jm = g.RT - 1;
+    g.arows = ((32 * (jm >> 4) + 16 + (jm & 15) + 1) + 7) / 8 * 8;
+  } else {
+    g.arows = 2 * ((g.RT + 7) / 8 * 8);
+  }
+  return g;
+}
+
 GuSlabGeom gu_slab_geom(int P, int D, int num_sms) {
   GuSlabGeom g{};
   g.P = P;
@@ -1692,13 +1730,7 @@ size_t dn_slab_elems(int D, int nR) {
 cudaError_t launch_build_slabs(const uint16_t* Wp, const int* rc, int nC, int nR, int D, int N, const GuSlabGeom& g,
                                uint16_t* gu_slab, uint16_t* dn_slab, unsigned* err, cudaStream_t st) {
   if (gu_slab && g.P > 0) {
-    const size_t chunks = gu_slab_elems(g) / 8;
-    const int grid = static_cast<int>(std::min<size_t>((chunks + 255) / 256, 152 * 16));
-    if (chunks < (size_t(1) << 31))
-      k_build_gu_slab<uint32_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
-    else
-      k_build_gu_slab<size_t><<<grid, 256, 0, st>>>(Wp, rc, D, N, g, gu_slab, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_build_gu_tiles(Wp, rc, D, N, g, 0, g.T, gu_slab, err, st);
     if (e != cudaSuccess) return e;
   }
   if (dn_slab && nR > 0) {

@@ -175,8 +175,12 @@ cudaError_t reset_counters(pop_ffn* h, cudaStream_t st) {
 cudaError_t skip_list_tail(pop_ffn* h, cudaStream_t st) {
   h->host_step = 0;
   if (h->cnt.n_R == 0) return cudaSuccess;
-  return cudaMemcpyAsync(h->rcs + h->cnt.k, h->rc + h->cnt.n_C, sizeof(int) * h->cnt.n_R, cudaMemcpyDeviceToDevice,
-                         st);
+  cudaError_t e = cudaMemcpyAsync(h->rcs + h->cnt.k, h->rc + h->cnt.n_C, sizeof(int) * h->cnt.n_R,
+                                  cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess || !h->gu_slab_skip) return e;
+  // the skip slab's R tiles (its selected tiles are rebuilt at every update step)
+  const GuSlabGeom& g = h->gu_geom_skip;
+  return launch_build_gu_tiles(h->Wp, h->rcs, h->D, h->N, g, g.Ts, g.T, h->gu_slab_skip, h->err, st);
 }
 
 // Rebuilds the B > 1 decode slabs from the current partition (stream-ordered after it).
@@ -428,7 +432,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
     h->gu_geom = gu_slab_geom(cnt.n_C + cnt.n_R, D, h->num_sms);
     POP_ALLOC(h->gu_slab, gu_slab_elems(h->gu_geom));
     if (cfg->skip && cfg->period > 1 && cnt.n_C > 0) {
-      h->gu_geom_skip = gu_slab_geom(cnt.k + cnt.n_R, D, h->num_sms);
+      h->gu_geom_skip = gu_slab_geom_split(cnt.k, cnt.k + cnt.n_R, D, h->num_sms);
       POP_ALLOC(h->gu_slab_skip, gu_slab_elems(h->gu_geom_skip));
     }
     POP_ALLOC(h->dn_slab, dn_slab_elems(D, cnt.n_R));
@@ -609,8 +613,8 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     prof_mark(h, 3, st);
     // skip variant, update step: a later B > 1 skip step streams the slab of this selection's list
     if (skip_mode && !skip && h->gu_slab_skip)
-      POP_CUDA(h, launch_build_slabs(h->Wp, h->rcs, k, nR, h->D, h->N, h->gu_geom_skip, h->gu_slab_skip, nullptr,
-                                     h->err, st));
+      POP_CUDA(h, launch_build_gu_tiles(h->Wp, h->rcs, h->D, h->N, h->gu_geom_skip, 0, h->gu_geom_skip.Ts,
+                                        h->gu_slab_skip, h->err, st));
     prof_mark(h, 4, st);
   } else {
     // gate/up, then the down GEMM over R and the selected items with the selection inside; a skip
@@ -626,8 +630,8 @@ pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* str
     // skip variant, update step: the slab of [C[S] | R] for the steps until the next update (an
     // ordinary launch: it starts once the selection's list is complete)
     if (skip_mode && !skip && h->gu_slab_skip)
-      POP_CUDA(h, launch_build_slabs(h->Wp, h->rcs, k, nR, h->D, h->N, h->gu_geom_skip, h->gu_slab_skip, nullptr,
-                                     h->err, st));
+      POP_CUDA(h, launch_build_gu_tiles(h->Wp, h->rcs, h->D, h->N, h->gu_geom_skip, 0, h->gu_geom_skip.Ts,
+                                        h->gu_slab_skip, h->err, st));
     prof_mark(h, 4, st);
   }
   prof_end(h);

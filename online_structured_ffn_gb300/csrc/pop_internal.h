@@ -96,8 +96,25 @@ cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int nu
 // gate rows fill rows [0, RT) and the up rows start at row round8(RT).
 struct GuSlabGeom {
   int P, T, RT, KB, arows, paired;
+  int Ts, P1;  // two regions: tiles [0, Ts) hold positions [0, P1), the rest [P1, P) (Ts = 0: one)
 };
+// List position held by row slot j of tile t, or -1 for an empty slot.
+__host__ __device__ inline int gu_slab_pos(const GuSlabGeom& g, int t, int j) {
+  if (j >= g.RT) return -1;
+  if (t < g.Ts) {
+    const int p = t * g.RT + j;
+    return p < g.P1 ? p : -1;
+  }
+  const int p = g.P1 + (t - g.Ts) * g.RT + j;
+  return p < g.P ? p : -1;
+}
 GuSlabGeom gu_slab_geom(int P, int D, int num_sms);
+// The same tiles for a list in two regions, [0, P1) and [P1, P), kept in separate tiles so that
+// the first region's tiles can be rebuilt alone.
+GuSlabGeom gu_slab_geom_split(int P1, int P, int D, int num_sms);
+// Builds tiles [t_lo, t_hi) of a gate/up slab from the packed weights and the list rc.
+cudaError_t launch_build_gu_tiles(const uint16_t* Wp, const int* rc, int D, int N, const GuSlabGeom& g, int t_lo,
+                                  int t_hi, uint16_t* gu_slab, unsigned* err, cudaStream_t st);
 size_t gu_slab_elems(const GuSlabGeom& g);
 // Down slab: the down columns of R in tiles of 64 items x 128 outputs (MN-major image: two halves of
 // 64 outputs, 64 items x 128 bytes each, 128-byte swizzle) at ((o * kbr + b) * 8192) elements for
