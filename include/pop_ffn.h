@@ -135,7 +135,11 @@ pop_status pop_set_partition(pop_ffn_t h, const int* R, const int* C, const int*
  * selection runs inside the gate/up kernel at B = 1 and inside the down kernel at B > 1, and at
  * B = 1 with |C| > 8192 as a third kernel between them). The next kernel's weight loads overlap
  * the previous kernel's tail; each kernel waits for its predecessor before it touches data a
- * previous call may still use.
+ * previous call may still use. Steps can be captured in a CUDA graph. With cfg.skip and
+ * period > 1 the steps between updates run over R and the held selection only; which steps those
+ * are is decided on the host (a counter reset by every partition call), so a captured graph
+ * replays the update/skip pattern it captured. At B > 1 an update step of the skip variant adds
+ * a third kernel that rebuilds the selected rows' tiles of the skip steps' slab.
  * STATE if no partition has been set. */
 pop_status pop_decode_step(pop_ffn_t h, const void* x, int B, void* y, void* stream);
 
