@@ -264,3 +264,28 @@ def test_moe_full_size(env):
         del Wg, W1, W2
     _decode_steps(env, m, parts, B, steps=2)
     m.close()
+
+
+def test_moe_many_experts(env):
+    """40 experts (more than the 32 warps that number the tokens per expert in one pass), a
+    100-token prompt (a few tokens per expert), and decode steps of 5 tokens (most experts idle)."""
+    _, torch, dev = env
+    E, D, N, M, B = 40, 64, 256, 100, 5
+    m = Moe(env, E, D, N, seed=7, r=0.3, gamma=0.1, max_batch=B, max_prefill_tokens=64)
+    X = synth.prompt(m.seed, M, m.sc)
+    L = synth.router_logits(m.seed, M, E).astype(np.float32)
+    Y = torch.empty((M, D), dtype=torch.float32, device=dev)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
+    m.moe.check()
+    ex = _check_routing(m.moe, L)
+    counts = np.bincount(ex.ravel(), minlength=E)
+    assert np.array_equal(m.moe.token_counts(), counts) and counts.sum() == 2 * M
+    ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, 0.3, 0.1)
+    for e in range(E):
+        p = ref["parts"][e]
+        bad, _, _ = parity.compare_partition(m.moe.experts[e].partition(), (p["R"], p["C"], p["P"]), p["I"],
+                                             p["counts"])
+        assert len(bad) == 0, f"expert {e}"
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64)
+    _decode_steps(env, m, ref["parts"], B, steps=2)
+    m.close()
