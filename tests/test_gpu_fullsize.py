@@ -41,17 +41,21 @@ def _layer(env, D, N, **kw):
     return ffn, (Wg, W1, W2), synth.dim_scales(0, D)
 
 
-def test_prefill_7b_sampled(env):
+@pytest.mark.parametrize("D,N,L,r,chunk,B", [(4096, 11008, 2048, 0.299, 2048, 1),
+                                             (4096, 11008, 16 * 1024, 0.5, 4096, 16),
+                                             (8192, 28672, 64 * 512, 0.5, 8192, 64)])
+def test_prefill_sampled(env, D, N, L, r, chunk, B):
+    """The prompts of the benchmark's workloads, in its chunking: 2048 tokens (7B, B=1), 16 x 1024
+    (7B, B=16), 64 x 512 (70B shape)."""
     _, torch, dev = env
-    D, N, L = 4096, 11008, 2048
-    ffn, (Wg, W1, W2), sc = _layer(env, D, N, r=0.299, gamma=0.1, max_batch=1, max_prefill_tokens=L)
+    ffn, (Wg, W1, W2), sc = _layer(env, D, N, r=r, gamma=0.1, max_batch=B, max_prefill_tokens=chunk)
     X = synth.prompt(0, L, sc)
     Y = torch.empty((L, D), dtype=torch.float32, device=dev)
     ffn.prefill_partition(up(env, X), Y)
     ffn.check()
     I, ss = ffn.importance()
     rng = np.random.default_rng(0)
-    ch = np.sort(rng.choice(N, 96, replace=False))
+    ch = np.sort(rng.choice(N, 64, replace=False))
     Xf = f64(X)
     Z = oracle.ffn_activations(f64(Wg[ch]), f64(W1[ch]), Xf)
     ss_ref, I_ref = oracle.channel_importance(f64(W2[:, ch]), Z)
@@ -65,7 +69,7 @@ def test_prefill_7b_sampled(env):
     assert np.all(np.abs(Yg - Yr) <= 2.0 ** -8 * (np.abs(Zr) @ np.abs(f64(W2)).T) + 1e-6)
     # property at full size: the split is the counting rule applied to the GPU's own importance
     R, C, P = ffn.partition()
-    R0, C0, P0 = oracle.partition(I, oracle.region_counts(N, 0.299, 0.1))
+    R0, C0, P0 = oracle.partition(I, oracle.region_counts(N, r, 0.1))
     assert np.array_equal(R, R0) and np.array_equal(C, C0) and np.array_equal(P, P0)
     ffn.close()
 
