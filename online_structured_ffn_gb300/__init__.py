@@ -133,6 +133,21 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
+def _expect(t, name, dtype, shape, min_rows=0):
+    """Checks a tensor argument before its address goes to the C ABI: dtype, contiguity and shape
+    (None in `shape` accepts any extent; an output may have more rows than it receives, at least
+    `min_rows`). Raises PopError(POP_ERR_INVALID_ARG)."""
+    if t is None:
+        return
+    ok = (t.dtype == dtype and t.is_contiguous() and t.dim() == len(shape)
+          and all(want is None or got == want for got, want in zip(t.shape, shape))
+          and (t.dim() == 0 or t.shape[0] >= min_rows))
+    if not ok:
+        raise PopError(POP_ERR_INVALID_ARG, f"{name}: expected a contiguous {dtype} tensor of shape "
+                                            f"{tuple('*' if w is None else w for w in shape)}, got "
+                                            f"{t.dtype} {tuple(t.shape)}{'' if t.is_contiguous() else ' (strided)'}")
+
+
 def _int_array(a):
     import numpy as np
     arr = np.ascontiguousarray(a, dtype=np.int32)
@@ -284,9 +299,14 @@ class PopFFN:
         return torch.float32 if self.cfg.out_f32 else torch.bfloat16
 
     def prefill_partition(self, X, Y=None, stream=None):
+        import torch
+        _expect(X, "X", torch.bfloat16, (None, self.D))
+        _expect(Y, "Y", self.out_dtype(), (None, self.D), X.shape[0])
         pop_prefill_partition(self.handle, X, X.shape[0], Y, stream)
 
     def partition_from_importance(self, importance, stream=None):
+        import torch
+        _expect(importance, "importance", torch.float32, (self.N,))
         pop_partition_from_importance(self.handle, importance, stream)
 
     def set_partition(self, R, C, P, stream=None):
@@ -294,15 +314,19 @@ class PopFFN:
 
     def decode_step(self, x, y=None, stream=None):
         import torch
+        _expect(x, "x", torch.bfloat16, (None, self.D))
         if y is None:
             y = torch.empty((x.shape[0], self.D), dtype=self.out_dtype(), device=x.device)
+        _expect(y, "y", self.out_dtype(), (None, self.D), x.shape[0])
         pop_decode_step(self.handle, x, x.shape[0], y, stream)
         return y
 
     def dense_ref(self, X, Y=None, stream=None):
         import torch
+        _expect(X, "X", torch.bfloat16, (None, self.D))
         if Y is None:
             Y = torch.empty((X.shape[0], self.D), dtype=self.out_dtype(), device=X.device)
+        _expect(Y, "Y", self.out_dtype(), (None, self.D), X.shape[0])
         pop_ffn_dense_ref(self.handle, X, X.shape[0], Y, stream)
         return Y
 
@@ -389,13 +413,20 @@ class PopMoE:
 
     def prefill_partition(self, X, logits, Y=None, stream=None):
         """X: bf16 [M, D]; logits: float32 [M, E]; Y (optional): [M, D] of out_dtype()."""
+        import torch
+        _expect(X, "X", torch.bfloat16, (None, self.D))
+        _expect(logits, "logits", torch.float32, (None, self.E), X.shape[0])
+        _expect(Y, "Y", self.out_dtype(), (None, self.D), X.shape[0])
         _check_moe(load_library().pop_moe_prefill_partition(self.handle, _ptr(X), _ptr(logits), X.shape[0], _ptr(Y),
                                                             _stream(stream)), self.handle)
 
     def decode_step(self, x, logits, y=None, stream=None):
         import torch
+        _expect(x, "x", torch.bfloat16, (None, self.D))
+        _expect(logits, "logits", torch.float32, (None, self.E), x.shape[0])
         if y is None:
             y = torch.empty((x.shape[0], self.D), dtype=self.out_dtype(), device=x.device)
+        _expect(y, "y", self.out_dtype(), (None, self.D), x.shape[0])
         _check_moe(load_library().pop_moe_decode_step(self.handle, _ptr(x), _ptr(logits), x.shape[0], _ptr(y),
                                                       _stream(stream)), self.handle)
         return y

@@ -134,3 +134,29 @@ def test_moe_rejects_bad_arguments_before_touching_cuda(pop):
     assert lib.pop_moe_expert(None, 0) is None
     assert lib.pop_moe_num_experts(None) == -1
     lib.pop_moe_destroy(None)  # no-op
+
+
+def test_binding_checks_tensor_arguments_before_the_c_abi(pop):
+    # the wrappers check dtype, contiguity and shape on the host; nothing reaches the library
+    torch = pytest.importorskip("torch")
+    f = pop.PopFFN.__new__(pop.PopFFN)
+    f.handle, f.D, f.N = None, 8, 16
+    f.cfg = pop.pop_config(D=8, D_FF=16, r=0.3, gamma=0.1, period=1, max_batch=4, max_prefill_tokens=8, out_f32=1)
+    good_x = torch.zeros((2, 8), dtype=torch.bfloat16)
+    for bad in (torch.zeros((2, 8), dtype=torch.float32), torch.zeros((2, 9), dtype=torch.bfloat16),
+                torch.zeros((8, 2), dtype=torch.bfloat16).t(), torch.zeros(8, dtype=torch.bfloat16)):
+        with pytest.raises(pop.PopError) as e:
+            f.decode_step(bad)
+        assert e.value.status == pop.POP_ERR_INVALID_ARG
+    with pytest.raises(pop.PopError):
+        f.decode_step(good_x, torch.zeros((2, 8), dtype=torch.bfloat16))  # y of the wrong dtype
+    with pytest.raises(pop.PopError):
+        f.partition_from_importance(torch.zeros(15, dtype=torch.float32))
+    m = pop.PopMoE.__new__(pop.PopMoE)
+    m.handle, m.D, m.N, m.E, m.cfg = None, 8, 16, 4, f.cfg
+    with pytest.raises(pop.PopError):
+        m.decode_step(good_x, torch.zeros((2, 4), dtype=torch.float64))  # logits must be float32
+    with pytest.raises(pop.PopError):
+        m.prefill_partition(good_x, torch.zeros((1, 4), dtype=torch.float32))  # a row per token
+    with pytest.raises(pop.PopError):
+        f.decode_step(good_x, torch.zeros((1, 8), dtype=torch.float32))  # y too short
