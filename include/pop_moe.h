@@ -58,7 +58,8 @@ pop_status pop_moe_prefill_partition(pop_moe_t m, const void* X, const float* lo
  * y device [B, D] (dtype per out_f32), 1 <= B <= max_batch. Every expert runs pop_decode_step on
  * a [B, D] input holding its routed tokens in ascending token order followed by zero rows (a zero
  * row has z = 0, so it changes neither the batch-max scores nor the routed tokens' outputs).
- * No allocation and no host synchronization: 2 + 2 * n_experts kernels on `stream`.
+ * No allocation and no host synchronization: 2 + 2 * n_experts kernels on `stream` (the skip
+ * variant's update steps add, per expert at B > 1, the rebuild of its slab's selected tiles).
  * STATE if no partition has been set. */
 pop_status pop_moe_decode_step(pop_moe_t m, const void* x, const float* logits, int B, void* y, void* stream);
 
