@@ -1,10 +1,12 @@
 """Parity at the workload sizes, in the launch configuration the benchmark uses.
 
-LLaMA-2-7B FFN shape (D=4096, D_FF=11008) with B=1 and B=16, and the LLaMA-70B FFN shape
-(D=8192, D_FF=28672) with B=64 and a period of 16. A full CPU prefill at these sizes is out of
-reach for the float64 oracle, so prefill is checked on sampled channels and tokens, plus the
-property that the GPU's R/C/P split is the counting rule applied to its own importance; decode
-steps are checked in full on a partition the oracle computes from a short prompt.
+LLaMA-2-7B FFN shape (D=4096, D_FF=11008) with B=1 and B=16 (also the static-mask and full
+re-evaluation comparators), and the LLaMA-70B FFN shape (D=8192, D_FF=28672) with B=64 and a
+period of 16, with and without the skip variant. A full CPU prefill at these sizes is out of
+reach for the float64 oracle, so each workload's prompt is checked on sampled channels and
+tokens, plus the property that the GPU's R/C/P split is the counting rule applied to its own
+importance; decode steps are checked in full on a partition the oracle computes from a short
+prompt (when a flagged near-tie went the other way, against the FFN over the GPU's own set).
 """
 import numpy as np
 import pytest
