@@ -528,49 +528,80 @@ def run_e2e(stack, steps):
 
 # ------------------------------------------------------------------ CPU oracle arm
 
-class OracleSample:
-    """The CPU oracle on one layer of a workload: weights and inputs are prepared once; `run`
-    times the oracle on a bounded sample (a few prompt tokens and decode steps) and extrapolates
-    linearly to one full session of that layer (all prompt tokens, all decode steps)."""
+# A prompt whose float64 prefill exceeds this many flops is timed at two sizes and fitted (a
+# fixed cost plus a cost per token) instead of in full.
+PREFILL_FULL_FLOP_LIMIT = 2.0e12
+PREFILL_FIT_SIZES = (256, 512)
 
-    def __init__(self, wl, seed=0, max_prefill=8, max_decode=4):
+
+class OracleSample:
+    """The CPU oracle on one layer of a workload (one expert of an MoE layer, with its expected
+    share of the tokens). `run` times, on the host cores:
+
+    * the prefill of the layer's whole prompt (all its prompt tokens), or, where that exceeds
+      PREFILL_FULL_FLOP_LIMIT, the prefill at two prompt lengths, fitted as a fixed cost plus a
+      cost per token and evaluated at the whole prompt;
+    * `decode_steps` decode steps, whose mean stands for each of the session's T steps (every
+      step does the same work);
+
+    and returns the session time these give, the wall time the sample itself took, and a
+    description. One layer's session is what the metric's unit (tokens/s per FFN layer) counts."""
+
+    def __init__(self, wl, seed=0, decode_steps=4):
         import oracle
         import synth
         self.wl, self.oracle = wl, oracle
         f64 = synth.bf16_to_f64
         D, N, B = wl["D"], wl["N"], wl["B"]
         self.E = wl.get("experts", 1)
-        # an MoE layer is sampled through one expert: its expected share of the tokens (2 of E
-        # experts per token), extrapolated to all E experts
-        self.share = 2.0 / self.E if self.E > 1 else 1.0
+        self.share = 2.0 / self.E if self.E > 1 else 1.0  # top-2 routing: 2 of E experts per token
         self.Bs = max(1, int(round(B * self.share)))
+        self.m_full = max(1, int(round(wl["M"] * self.share)))
+        self.fit = 6.0 * self.m_full * D * N > PREFILL_FULL_FLOP_LIMIT
+        self.sizes = PREFILL_FIT_SIZES if self.fit else (self.m_full,)
+        self.d = decode_steps
         self.W = tuple(f64(w) for w in synth.ffn_weights(seed, D, N))
         sc = synth.dim_scales(seed, D)
-        self.X = f64(synth.prompt(seed, max_prefill, sc))
-        self.xs = [f64(synth.decode_input(seed, t, self.Bs, sc)) for t in range(max_decode)]
+        self.X = f64(synth.prompt(seed, max(self.sizes), sc))
+        self.xs = [f64(synth.decode_input(seed, t, self.Bs, sc)) for t in range(decode_steps)]
 
-    def run(self, prefill_tokens, decode_steps):
+    def run(self):
         wl, oracle = self.wl, self.oracle
         Wg, W1, W2 = self.W
-        t0 = time.perf_counter()
-        pre = oracle.prefill(Wg, W1, W2, self.X[:prefill_tokens], wl["r"], wl["gamma"])
-        t_pre = time.perf_counter() - t0
+        t_start = time.perf_counter()
+        t_at = {}
+        pre = None
+        for m in self.sizes:
+            t0 = time.perf_counter()
+            pre = oracle.prefill(Wg, W1, W2, self.X[:m], wl["r"], wl["gamma"])
+            t_at[m] = time.perf_counter() - t0
+        if self.fit:
+            m1, m2 = self.sizes
+            per_tok = (t_at[m2] - t_at[m1]) / (m2 - m1)
+            fixed = t_at[m1] - per_tok * m1
+            t_pre = fixed + per_tok * self.m_full
+            pre_info = (f"prefill timed at {m1} and {m2} prompt tokens ({t_at[m1]:.2f} s, {t_at[m2]:.2f} s) and "
+                        f"fitted as {fixed:.3f} s + {1e3 * per_tok:.3f} ms per token, evaluated at its "
+                        f"{self.m_full} prompt tokens ({t_pre:.2f} s)")
+        else:
+            t_pre = t_at[self.m_full]
+            pre_info = f"prefill of all its {self.m_full} prompt tokens timed ({t_pre:.2f} s)"
         sess = oracle.PopSession(Wg, W1, W2, pre["R"], pre["C"], pre["counts"].k, period=wl["period"])
         t0 = time.perf_counter()
-        for x in self.xs[:decode_steps]:
+        for x in self.xs:
             sess.step(x)
-        t_dec = (time.perf_counter() - t0) / decode_steps
-        session = self.E * (t_pre * wl["M"] * self.share / prefill_tokens + t_dec * wl["T"])
+        t_dec = (time.perf_counter() - t0) / len(self.xs)
+        wall = time.perf_counter() - t_start
+        session = t_pre + t_dec * wl["T"]
+        what = (f"one expert ({wl['D']}x{wl['N']}) of the {self.E}-expert MoE layer with its expected share of "
+                f"the tokens" if self.E > 1 else f"one layer of the {wl['D']}x{wl['N']} FFN")
+        info = (f"{what}: {pre_info}; {self.d} decode steps at B={self.Bs} timed ({t_dec:.3f} s each), "
+                f"their mean taken for each of the session's {wl['T']} steps; float64 numpy with its default "
+                f"BLAS threading")
         if self.E > 1:
-            info = (f"one of {self.E} experts ({wl['D']}x{wl['N']}) of the MoE layer: oracle prefill of "
-                    f"{prefill_tokens} of its ~{wl['M'] * self.share:.0f} routed prompt tokens ({t_pre:.2f} s) and "
-                    f"{decode_steps} of {wl['T']} decode steps at its ~{self.Bs} routed tokens ({t_dec:.2f} s each), "
-                    f"extrapolated linearly to one full session of all {self.E} experts")
-        else:
-            info = (f"one layer of the {wl['D']}x{wl['N']} FFN: oracle prefill of {prefill_tokens} of {wl['M']} "
-                    f"prompt tokens ({t_pre:.2f} s) and {decode_steps} of {wl['T']} decode steps at B={wl['B']} "
-                    f"({t_dec:.2f} s each), extrapolated linearly to one full session")
-        return session, info
+            # the layer's session: every expert runs its share (the metric counts tokens per layer)
+            session *= self.E
+        return session, wall, info
 
 
 def host_threads():
@@ -580,10 +611,13 @@ def host_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl):
-    session, info = OracleSample(wl).run(prefill_tokens=8, decode_steps=4)
+def cpu_baseline(wl, repeats=3):
+    """The oracle's sample (OracleSample), run `repeats` times; the median session time."""
+    sample = OracleSample(wl)
+    runs = [sample.run() for _ in range(repeats)]
+    session = statistics.median(r[0] for r in runs)
     return {"value": wl["B"] * wl["T"] / session, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
-            "sample": info + "; float64 numpy with its default BLAS threading"}
+            "sample": runs[-1][2] + f"; median of {repeats} runs"}
 
 
 # ------------------------------------------------------------------ main
@@ -654,20 +688,22 @@ def main():
         if rank != 0:
             return
         t0 = time.perf_counter()
-        sample = OracleSample(wl, max_prefill=2, max_decode=1)
+        sample = OracleSample(wl)
         for _ in range(args.warmup):
-            sample.run(2, 1)
-        times, info = [], ""
+            sample.run()
+        sessions, walls, info = [], [], ""
         for _ in range(args.steps):
-            s, info = sample.run(2, 1)
-            times.append(s)
-        value = wl["B"] * wl["T"] * len(times) / sum(times)
+            sess_s, wall_s, info = sample.run()
+            sessions.append(sess_s)
+            walls.append(wall_s)
+        # each step is one timed sample; its value is the session those timings give (one layer)
+        value = wl["B"] * wl["T"] * len(sessions) / sum(sessions)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(walls) / len(walls),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
-                                 "sample": info + " (each step)"},
+                                 "sample": info + " (each step; ms_per_step is the wall time of one sample)"},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
         print(json.dumps(line), flush=True)

@@ -205,7 +205,9 @@ const char* pop_last_error(pop_ffn_t h);
  * The first call on each device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Errors: INVALID_ARG (NULL or misaligned pointer, D or D_FF outside the limits above, with the
- * message in pop_last_error(NULL)), UNSUPPORTED (not sm_103), CUDA. Calls no cudaMalloc/cudaFree. */
+ * message in pop_last_error(NULL)), UNSUPPORTED (not sm_103, or a device ordinal of 64 or more),
+ * CUDA (also when a CUDA error from the caller's earlier work is still pending on the thread:
+ * nothing is launched and that error is left in place). Calls no cudaMalloc/cudaFree. */
 pop_status pop_ffn_dense_token_noalloc(const void* Wg, const void* W1, const void* W2, int D, int D_FF,
                                        const void* x, void* y, int out_f32, void* stream);
 

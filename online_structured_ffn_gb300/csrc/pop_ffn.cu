@@ -23,7 +23,7 @@ struct pop_ffn {
   // packed weights and norms
   uint16_t* Wp = nullptr;
   float* n2 = nullptr;
-  // prefill scratch
+  // prefill scratch: z of one chunk as two bf16 planes, hi at Z, lo at Z + Mcap * ldZ
   uint16_t* Z = nullptr;
   int ldZ = 0, Mcap = 0;
   float* part = nullptr;
@@ -412,7 +412,7 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   } while (0)
   POP_ALLOC(h->Wp, static_cast<size_t>(N) * 3 * D);
   POP_ALLOC(h->n2, N);
-  POP_ALLOC(h->Z, static_cast<size_t>(h->Mcap) * h->ldZ);
+  POP_ALLOC(h->Z, 2 * static_cast<size_t>(h->Mcap) * h->ldZ);
   POP_ALLOC(h->part, static_cast<size_t>(h->Mcap / 32) * h->ldPart);
   POP_ALLOC(h->sumsq, N);
   POP_ALLOC(h->I, N);
@@ -495,16 +495,17 @@ static pop_status prefill_gemms(pop_ffn* h, const uint16_t* X, int M, void* Y, b
   const size_t esz = h->cfg.out_f32 ? 4 : 2;
   for (int c0 = 0; c0 < M; c0 += h->Mcap) {
     const int Mc = std::min(h->Mcap, M - c0);
-    CUtensorMap xm, zm;
+    uint16_t* Zlo = h->Z + static_cast<size_t>(h->Mcap) * h->ldZ;
+    CUtensorMap xm, zm, zlm;
     if (!encode_x_map(&xm, X + static_cast<size_t>(c0) * h->D, Mc, h->D) ||
-        !encode_z_map(&zm, h->Z, Mc, h->N, h->ldZ))
+        !encode_z_map(&zm, h->Z, Mc, h->N, h->ldZ) || !encode_z_map(&zlm, Zlo, Mc, h->N, h->ldZ))
       return fail(h, POP_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    POP_CUDA(h, launch_prefill_gateup(xm, h->maps, Mc, h->N, h->D, h->Z, h->ldZ, h->part, h->ldPart, h->err,
+    POP_CUDA(h, launch_prefill_gateup(xm, h->maps, Mc, h->N, h->D, h->Z, Zlo, h->ldZ, h->part, h->ldPart, h->err,
                                       h->wait_ns, h->num_sms, st));
     if (fold)
       POP_CUDA(h, launch_fold_sumsq(h->part, 4 * ((Mc + 127) / 128), h->ldPart, h->N, h->sumsq, c0 > 0 ? 1 : 0, st));
     if (Y)
-      POP_CUDA(h, launch_prefill_down(zm, h->maps, Mc, h->N, h->D,
+      POP_CUDA(h, launch_prefill_down(zm, zlm, h->maps, Mc, h->N, h->D,
                                       static_cast<uint8_t*>(Y) + static_cast<size_t>(c0) * h->D * esz,
                                       h->cfg.out_f32, h->err, h->wait_ns, h->num_sms, st));
   }

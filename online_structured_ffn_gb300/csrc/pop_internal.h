@@ -211,13 +211,15 @@ struct PrefillMaps {
 bool encode_weight_maps(PrefillMaps* m, const uint16_t* Wp, int D, int N);
 bool encode_x_map(CUtensorMap* m, const uint16_t* X, int M, int D);
 bool encode_z_map(CUtensorMap* m, const uint16_t* Z, int M, int N, int ldZ);
-// Z[m][n] = bf16(SiLU(X Wg^T) * (X W1^T)); part[(m/32)][n] = sum over 32 rows of z^2 (fp32, un-rounded z).
+// z = SiLU(X Wg^T) * (X W1^T) as two bf16 planes: Z[m][n] = bf16(z), Zlo[m][n] = bf16(z - Z[m][n]);
+// part[(m/32)][n] = sum over 32 rows of z^2 (fp32, un-rounded z).
 cudaError_t launch_prefill_gateup(const CUtensorMap& x_map, const PrefillMaps& maps, int M, int N, int D,
-                                  uint16_t* Z, int ldZ, float* part, int ldPart, unsigned* err, uint64_t wait_ns,
-                                  int num_sms, cudaStream_t st);
-// Y = Z W2^T, Y fp32 or bf16 [M, D].
-cudaError_t launch_prefill_down(const CUtensorMap& z_map, const PrefillMaps& maps, int M, int N, int D, void* Y,
-                                int out_f32, unsigned* err, uint64_t wait_ns, int num_sms, cudaStream_t st);
+                                  uint16_t* Z, uint16_t* Zlo, int ldZ, float* part, int ldPart, unsigned* err,
+                                  uint64_t wait_ns, int num_sms, cudaStream_t st);
+// Y = (Z + Zlo) W2^T, Y fp32 or bf16 [M, D] (z_map, zlo_map: the two planes, encode_z_map).
+cudaError_t launch_prefill_down(const CUtensorMap& z_map, const CUtensorMap& zlo_map, const PrefillMaps& maps,
+                                int M, int N, int D, void* Y, int out_f32, unsigned* err, uint64_t wait_ns,
+                                int num_sms, cudaStream_t st);
 size_t prefill_smem_bytes();
 
 // Sets the message that pop_last_error(NULL) returns on this thread.

@@ -7,17 +7,21 @@
 //
 // Kernel 1 (gate/up): for a tile of 128 tokens x 128 channels one UMMA of shape M=128, N=256
 // computes gate (columns 0..127) and up (128..255) together: the B tile stacks 128 Wg rows on
-// 128 W1 rows. The epilogue forms z = SiLU(g) * u in fp32, stores Z in bf16 for the down GEMM,
-// and reduces z^2 (from the un-rounded fp32 z) over each warp's 32 rows with a butterfly
-// reduce-scatter, writing one partial row per 32 tokens (deterministic; folded later).
-// Kernel 2 (down): Y = Z W2^T with M=128 tokens, N=256 outputs; the W2 operand comes straight
-// from the channel-major packed rows, so it is MN-major (d contiguous) in shared memory.
+// 128 W1 rows. The epilogue forms z = SiLU(g) * u in fp32 and stores it for the down GEMM as two
+// bf16 planes, hi = bf16(z) and lo = bf16(z - hi) (together about 16 significant bits, so y keeps
+// z's fp32 precision); it reduces z^2 (from the un-rounded fp32 z) over each warp's 32 rows with a
+// butterfly reduce-scatter, writing one partial row per 32 tokens (deterministic; folded later).
+// Kernel 2 (down): Y = Z W2^T = Z_hi W2^T + Z_lo W2^T with M=128 tokens, N=256 outputs; a stage
+// holds the hi and lo tiles of one k-block and one W2 tile that both MMAs read. The W2 operand
+// comes straight from the channel-major packed rows, so it is MN-major (d contiguous) in shared
+// memory.
 //
 // Both kernels are persistent (at most one CTA per SM), warp-specialised (warp 0 TMA producer,
-// warp 1 MMA issuer and TMEM owner, warps 2..5 epilogue), with a 4-stage TMA ring of 48 KB stages
-// and two 256-column TMEM accumulators so that the epilogue of tile i overlaps the MMAs of tile
-// i+1. Every mbarrier wait is bounded; on a time-out the CTA records DEVERR_TIMEOUT_*, stops
-// issuing, waits (bounded) for its TMA copies and MMAs in flight, frees TMEM and returns.
+// warp 1 MMA issuer and TMEM owner, warps 2..5 epilogue), with a TMA ring of 192 KB (4 stages of
+// 48 KB for gate/up, 3 of 64 KB for down) and two 256-column TMEM accumulators so that the
+// epilogue of tile i overlaps the MMAs of tile i+1. Every mbarrier wait is bounded; on a time-out
+// the CTA records DEVERR_TIMEOUT_*, stops issuing, waits (bounded) for its TMA copies and MMAs in
+// flight, frees TMEM and returns.
 #include "pop_device.cuh"
 #include "pop_internal.h"
 
@@ -26,11 +30,19 @@ namespace pop {
 namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 4;
 constexpr int THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = 256 * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+// gate/up: [A | B] x 4 stages; down: [A hi | A lo | B] x 3 stages (192 KB either way)
+template <int MODE>
+struct Ring {
+  static constexpr int stages = MODE == 0 ? 4 : 3;
+  static constexpr uint32_t a_planes = MODE == 0 ? 1u : 2u;
+  static constexpr uint32_t stage_bytes = a_planes * A_BYTES + B_BYTES;
+};
+constexpr uint32_t RING_BYTES = 4 * (A_BYTES + B_BYTES);
+static_assert(Ring<1>::stages * Ring<1>::stage_bytes == RING_BYTES, "both modes use the same ring");
 constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
 constexpr int GU_BN = 128;           // channels per gate/up tile
 constexpr int DN_BN = 256;           // outputs per down tile
@@ -40,30 +52,36 @@ constexpr int DN_BN = 256;           // outputs per down tile
 constexpr uint64_t DRAIN_NS = 1000000000ull;
 
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Ctl);
+constexpr size_t SMEM_BYTES = 1024 + RING_BYTES + sizeof(Ctl);
 }  // namespace
 
 size_t prefill_smem_bytes() { return SMEM_BYTES; }
 
 __device__ __forceinline__ float silu_p(float g) { return g / (1.0f + expf(-g)); }
 
-template <int MODE>  // 0 = gate/up, 1 = down
+// MODE 0 (gate/up): mapA = X, mapB0 = Wg, mapB1 = W1; writes Z (hi plane) and Zlo, and part.
+// MODE 1 (down): mapA = Z hi plane, mapA2 = Z lo plane, mapB0 = W2; writes Y.
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_prefill_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
-                   const __grid_constant__ CUtensorMap mapB1, int M, int Nout, int K, uint16_t* __restrict__ Z,
-                   int ldZ, float* __restrict__ part, int ldPart, void* __restrict__ Y, int out_f32,
+    k_prefill_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
+                   const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1, int M,
+                   int Nout, int K, uint16_t* __restrict__ Z, uint16_t* __restrict__ Zlo, int ldZ,
+                   float* __restrict__ part, int ldPart, void* __restrict__ Y, int out_f32,
                    unsigned* __restrict__ err, uint64_t wait_ns) {
+  constexpr int STAGES = Ring<MODE>::stages;
+  constexpr uint32_t STAGE_BYTES = Ring<MODE>::stage_bytes;
+  constexpr uint32_t B_OFF = Ring<MODE>::a_planes * A_BYTES;  // B tile within a stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int BN = MODE == 0 ? GU_BN : DN_BN;
@@ -108,6 +126,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&mapA);
       prefetch_tmap(&mapB0);
       if (MODE == 0) prefetch_tmap(&mapB1);
+      if (MODE == 1) prefetch_tmap(&mapA2);
       uint32_t issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -122,9 +141,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           uint8_t* sa = smem + s * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
+          uint8_t* sb = sa + B_OFF;
           mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);
           tma_load_2d(sa, &mapA, &ctl->full[s], kb * BK, m0);
+          if (MODE == 1) tma_load_2d(sa + A_BYTES, &mapA2, &ctl->full[s], kb * BK, m0);
           if (MODE == 0) {
             tma_load_2d(sb, &mapB0, &ctl->full[s], kb * BK, n0);
             tma_load_2d(sb + B_BYTES / 2, &mapB1, &ctl->full[s], kb * BK, n0);
@@ -169,13 +189,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + B_OFF;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t adesc = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
             const uint64_t bdesc = MODE == 0 ? smem_desc_sw128(sb + 32u * k, 16u, 1024u)
                                              : smem_desc_sw128(sb + 2048u * k, B_BYTES / 4, 1024u);
             umma_f16(d_tmem, adesc, bdesc, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+            if (MODE == 1)  // the lo plane against the same W2 tile
+              umma_f16(d_tmem, smem_desc_sw128(sa + A_BYTES + 32u * k, 16u, 1024u), bdesc, IDESC, 1u);
           }
           umma_commit(&ctl->empty[s]);
           ++consumed;
@@ -217,11 +239,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           float zv[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) zv[j] = silu_p(__uint_as_float(gr[j])) * __uint_as_float(ur[j]);
-          uint4* zp = reinterpret_cast<uint4*>(Z + static_cast<size_t>(row) * ldZ + n0 + c);
+          const size_t zoff = static_cast<size_t>(row) * ldZ + n0 + c;
+          uint4* zp = reinterpret_cast<uint4*>(Z + zoff);
+          uint4* zlp = reinterpret_cast<uint4*>(Zlo + zoff);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            zp[v] = make_uint4(pack_bf16x2(zv[8 * v], zv[8 * v + 1]), pack_bf16x2(zv[8 * v + 2], zv[8 * v + 3]),
-                               pack_bf16x2(zv[8 * v + 4], zv[8 * v + 5]), pack_bf16x2(zv[8 * v + 6], zv[8 * v + 7]));
+          for (int v = 0; v < 4; ++v) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float a = zv[8 * v + 2 * j], b = zv[8 * v + 2 * j + 1];
+              hw[j] = pack_bf16x2(a, b);
+              // z - hi is exact in fp32; its bf16 rounding leaves at most 2^-9 of it
+              lw[j] = pack_bf16x2(a - bf16lo(hw[j]), b - bf16hi(hw[j]));
+            }
+            zp[v] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            zlp[v] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) zv[j] *= zv[j];
           // butterfly reduce-scatter over the 32 rows: lane l ends with column l's sum
@@ -335,27 +368,28 @@ bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, in
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_prefill_gateup(const CUtensorMap& x_map, const PrefillMaps& maps, int M, int N, int D,
-                                  uint16_t* Z, int ldZ, float* part, int ldPart, unsigned* err, uint64_t wait_ns,
-                                  int num_sms, cudaStream_t st) {
+                                  uint16_t* Z, uint16_t* Zlo, int ldZ, float* part, int ldPart, unsigned* err,
+                                  uint64_t wait_ns, int num_sms, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(k_prefill_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int tiles = ((M + BM - 1) / BM) * ((N + GU_BN - 1) / GU_BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_prefill_gemm<0><<<grid, THREADS, SMEM_BYTES, st>>>(x_map, maps.wg, maps.w1, M, N, D, Z, ldZ, part, ldPart,
-                                                       nullptr, 0, err, wait_ns);
+  k_prefill_gemm<0><<<grid, THREADS, SMEM_BYTES, st>>>(x_map, x_map, maps.wg, maps.w1, M, N, D, Z, Zlo, ldZ, part,
+                                                       ldPart, nullptr, 0, err, wait_ns);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_down(const CUtensorMap& z_map, const PrefillMaps& maps, int M, int N, int D, void* Y,
-                                int out_f32, unsigned* err, uint64_t wait_ns, int num_sms, cudaStream_t st) {
+cudaError_t launch_prefill_down(const CUtensorMap& z_map, const CUtensorMap& zlo_map, const PrefillMaps& maps,
+                                int M, int N, int D, void* Y, int out_f32, unsigned* err, uint64_t wait_ns,
+                                int num_sms, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(k_prefill_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int tiles = ((M + BM - 1) / BM) * ((D + DN_BN - 1) / DN_BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_prefill_gemm<1><<<grid, THREADS, SMEM_BYTES, st>>>(z_map, maps.w2, maps.w2, M, D, N, nullptr, 0, nullptr, 0, Y,
-                                                       out_f32, err, wait_ns);
+  k_prefill_gemm<1><<<grid, THREADS, SMEM_BYTES, st>>>(z_map, zlo_map, maps.w2, maps.w2, M, D, N, nullptr, nullptr, 0,
+                                                       nullptr, 0, Y, out_f32, err, wait_ns);
   return cudaGetLastError();
 }
 

@@ -120,8 +120,13 @@ pop_status pop_ffn_dense_token_noalloc(const void* Wg, const void* W1, const voi
   if (!aligned16s(Wg) || !aligned16s(W1) || !aligned16s(W2) || !aligned16s(x) || !aligned16s(y))
     return static_fail(POP_ERR_INVALID_ARG, "dense_token_noalloc: pointers must be 16-byte aligned");
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return static_fail(POP_ERR_CUDA, "dense_token_noalloc: cudaGetDevice failed");
+  if (cudaGetDevice(&dev) != cudaSuccess) return static_fail(POP_ERR_CUDA, "dense_token_noalloc: cudaGetDevice failed");
+  if (dev < 0 || dev >= kMaxDevices)
+    return static_fail(POP_ERR_UNSUPPORTED, "dense_token_noalloc: device ordinal beyond the 64 this entry point tracks");
+  // an error left by the caller's own earlier work is reported as such, not as this call's launch
+  // failure (and is left in place for the caller)
+  if (cudaPeekAtLastError() != cudaSuccess)
+    return static_fail(POP_ERR_CUDA, "dense_token_noalloc: a CUDA error from earlier work is pending on this thread");
   float* z = nullptr;
   {
     // first call on this device: look up the device address of the static array (host code only

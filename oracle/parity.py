@@ -5,11 +5,16 @@ Acceptance (the method's own tolerance statement for this build):
   channels whose oracle score lies within FLAG_REL (1e-4) relative of the
   cut-off score; those are flagged and counted, not failed;
 * FFN outputs: relative L2 error <= 5e-3 and max abs error <= 2e-2 against the
-  oracle on the same bf16 inputs.
+  oracle on the same bf16 inputs. Every output is held to this, the prefill's
+  included. When a flagged near-tie went the other way, the GPU's output is
+  checked against the FFN over the set the GPU kept (``y_on_set``), so that no
+  step goes unchecked.
 """
 from __future__ import annotations
 
 import numpy as np
+
+from . import down_projection, ffn_activations
 
 FLAG_REL = 1e-4
 Y_REL_L2 = 5e-3
@@ -84,3 +89,12 @@ def compare_selection(S_gpu, S_ref, C, scores_ref, k):
     pos = {ch: p for p, ch in enumerate(np.asarray(C).tolist())}
     bad = [ch for ch in diff if ch not in pos or not flagged[pos[ch]]]
     return bad, int(flagged.sum()), len(diff)
+
+
+def y_on_set(Wg, W1, W2, channels, x):
+    """The FFN output over a fixed kept set of channels ("Overall framework": the final FFN runs
+    on R plus the selected candidates), for a step whose set differs from the oracle's own only
+    by flagged near-ties."""
+    keep = np.sort(np.asarray(channels, dtype=np.int64))
+    Z = ffn_activations(Wg[keep], W1[keep], x)
+    return down_projection(W2[:, keep], Z)

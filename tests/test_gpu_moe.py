@@ -1,7 +1,8 @@
 """MoE layer of POP-pruned experts on the GPU against the oracle (top-2 routing, per-expert
 partition from the routed prompt tokens, per-expert decode on routed tokens, weighted combine).
 
-Tiny layers are checked in full; the 8-expert D=4096, D_FF=14336 layer with a 4096-token prompt and
+Every output (prefill Y and decode y) is held to rel-L2 5e-3 and max-abs 2e-2. Tiny layers are
+checked in full; the 8-expert D=4096, D_FF=14336 layer with a 4096-token prompt and
 B=32 decode steps is checked on its routing (every token, exact), the counting rule on each
 expert's own importance, sampled channels and rows of the prefill, and full decode steps on
 partitions the oracle computes from a short prompt.
@@ -56,25 +57,9 @@ class Moe:
         self.moe.close()
 
 
-def _check_prefill_y(Y, Y_ref, X, L, w64, rows=None, what="MoE prefill Y", bf16_out=False):
-    """Prefill Y is made from bf16-rounded Z (the down GEMM's operand): rel-L2 <= 5e-3 and, per
-    element, |Y - Y_ref| <= sum over the token's experts of w * 2^-8 (|Z| |W2|^T), the bf16
-    rounding bound of a single layer's prefill weighted like the outputs (plus 2^-8 |Y| when the
-    output itself is rounded to bf16)."""
-    ex, w = oracle.moe_route(np.asarray(L, dtype=np.float32))
-    rows = np.arange(X.shape[0]) if rows is None else np.asarray(rows)
-    bound = np.zeros((len(rows), X.shape[1]))
-    for e in sorted(set(ex[rows].ravel().tolist())):
-        Wg, W1, W2 = w64(e)
-        for i, t in enumerate(rows):
-            for j in range(2):
-                if ex[t, j] == e:
-                    Z = oracle.ffn_activations(Wg, W1, f64(X[t:t + 1]))
-                    bound[i] += w[t, j] * 2.0 ** -8 * (np.abs(Z) @ np.abs(W2).T)[0]
-    if bf16_out:
-        bound += 2.0 ** -8 * np.abs(Y_ref)
-    assert parity.rel_l2(Y, Y_ref) <= parity.Y_REL_L2, what
-    assert np.all(np.abs(Y - Y_ref) <= bound + 1e-6), f"{what}: max excess {np.max(np.abs(Y - Y_ref) - bound):.3e}"
+def _check_prefill_y(Y, Y_ref, what="MoE prefill Y"):
+    """Prefill Y against the oracle: rel-L2 <= 5e-3 and max-abs <= 2e-2, like every output."""
+    parity.check_y(Y, Y_ref, what)
 
 
 def _check_routing(moe, L):
@@ -109,11 +94,23 @@ def _decode_steps(env, m, parts, B, steps, check_sel=True):
                 if nd:
                     flipped.add(e)
         flips += len(flipped)
-        rows = [b for b in range(B) if not (set(ex[b].tolist()) & flipped)]
-        parity.check_y(y[rows], ys_ref[t][rows], f"B={B} step {t}")
+        y_ref = ys_ref[t].copy()
+        if flipped:
+            # a flagged near-tie went the other way in these experts: the rows they serve are checked
+            # against the weighted FFNs over the sets the GPU kept
+            _, w = oracle.moe_route(Ls[t])
+            for b in range(B):
+                if set(ex[b].tolist()) & flipped:
+                    y_ref[b] = 0.0
+                    for j in range(2):
+                        e = int(ex[b, j])
+                        keep = np.concatenate([parts[e]["R"], m.moe.experts[e].selected()])
+                        y_ref[b] += w[b, j] * parity.y_on_set(*m.w64(e), keep, f64(xs[t][b:b + 1]))[0]
+        parity.check_y(y, y_ref, f"B={B} step {t}")
     for e in range(m.E):
         assert m.moe.experts[e].step_count() == steps
     m.moe.check()
+    print(f"[flags] MoE decode E={m.E} D={m.D} N={m.N} B={B}: {steps} steps, expert selections flipped {flips}")
     return flips
 
 
@@ -135,7 +132,7 @@ def test_moe_prefill_and_decode(env, B):
         bad, _, _ = parity.compare_partition(m.moe.experts[e].partition(), (p["R"], p["C"], p["P"]), p["I"],
                                              p["counts"])
         assert len(bad) == 0, f"expert {e}: partition differs outside the flagged band: {bad[:10]}"
-    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64)
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"])
     _decode_steps(env, m, ref["parts"], B, steps=4)
     m.close()
 
@@ -160,7 +157,7 @@ def test_moe_idle_experts(env):
         assert C.tolist() == list(range(c.n_R, N - c.n_P))
         assert P.tolist() == list(range(N - c.n_P, N))
     ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, 0.3, 0.1)
-    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64, what="MoE prefill Y with idle experts")
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"], what="MoE prefill Y with idle experts")
     x = synth.decode_input(m.seed, 0, B, m.sc)
     Lt = np.full((B, E), -4.0, dtype=np.float32)
     Lt[:, 1], Lt[:, 0] = 2.0, 1.0
@@ -188,8 +185,7 @@ def test_moe_bf16_output_and_errors(env):
     Y = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
     m.moe.prefill_partition(up(env, X), logits_t(env, L), Y)
     ref = oracle.moe_prefill([m.w64(e) for e in range(E)], f64(X), L, 0.299, 0.1)
-    _check_prefill_y(Y.float().cpu().numpy(), ref["Y"], X, L, m.w64, what="MoE prefill Y (bf16 out)",
-                     bf16_out=True)
+    _check_prefill_y(Y.float().cpu().numpy(), ref["Y"], what="MoE prefill Y (bf16 out)")
     with pytest.raises(pop.PopError) as err:
         m.moe.decode_step(up(env, np.concatenate([x, x])), logits_t(env, np.concatenate([Lx, Lx])))
     assert err.value.status == pop.POP_ERR_INVALID_ARG  # B > max_batch
@@ -223,7 +219,6 @@ def test_moe_full_size(env):
     rows = np.sort(rng.choice(M, 3, replace=False))
     Yg = Y.cpu().numpy()[rows]
     Yr = np.zeros((len(rows), D))
-    bound = np.zeros((len(rows), D))
     Xf = f64(X)
     for e in range(E):
         R, C, P = m.moe.experts[e].partition()
@@ -242,11 +237,8 @@ def test_moe_full_size(env):
                 if ex[t, j] == e:
                     Z = oracle.ffn_activations(Wg, W1, Xf[t:t + 1])
                     Yr[i] += w_ref[t, j] * oracle.down_projection(W2, Z)[0]
-                    bound[i] += w_ref[t, j] * 2.0 ** -8 * (np.abs(Z) @ np.abs(W2).T)[0]
         del Wg, W1, W2
-    # prefill Y comes from bf16-rounded Z: the single-layer prefill bound, weighted like the outputs
-    assert parity.rel_l2(Yg, Yr) <= parity.Y_REL_L2
-    assert np.all(np.abs(Yg - Yr) <= bound + 1e-6), f"max excess {np.max(np.abs(Yg - Yr) - bound):.3e}"
+    _check_prefill_y(Yg, Yr, "MoE prefill Y, sampled rows")
     # decode on partitions the oracle takes from a short prompt (8 tokens, top-2: some experts idle)
     Xs = synth.prompt(m.seed, 8, m.sc)
     Ls = L[:8]
@@ -286,6 +278,6 @@ def test_moe_many_experts(env):
         bad, _, _ = parity.compare_partition(m.moe.experts[e].partition(), (p["R"], p["C"], p["P"]), p["I"],
                                              p["counts"])
         assert len(bad) == 0, f"expert {e}"
-    _check_prefill_y(Y.cpu().numpy(), ref["Y"], X, L, m.w64)
+    _check_prefill_y(Y.cpu().numpy(), ref["Y"])
     _decode_steps(env, m, ref["parts"], B, steps=2)
     m.close()

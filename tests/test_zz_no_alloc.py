@@ -3,14 +3,14 @@
 Some callers cannot allocate GPU memory while they run (their device memory is reserved up
 front by their own memory manager, or their loop must not enter the CUDA allocator), so
 pop_ffn_dense_token_noalloc keeps its scratch in a static device array instead. Its output must
-agree with the handle-based dense path (pop_ffn_dense_ref) on the same weights, on two calls in
-a row that share that array. This file is collected last on purpose.
+agree with the handle-based dense path (pop_ffn_dense_ref) on the same weights, and with the CPU
+oracle's dense FFN, on two calls in a row that share that array. This file is collected last on
+purpose.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from oracle import parity
 
@@ -52,7 +52,10 @@ def test_noalloc_matches_dense_ref_twice(env, D, N, out_f32):
         torch.cuda.synchronize()
         a, b = y.float().cpu().numpy(), y_ref.float().cpu().numpy()
         assert np.all(np.isfinite(a))
-        parity.check_y(a, b, f"no-alloc call {step}")
+        parity.check_y(a, b, f"no-alloc call {step} against pop_ffn_dense_ref")
+        f64 = synth.bf16_to_f64
+        y_or = oracle.dense_ffn(f64(Wg), f64(W1), f64(W2), f64(synth.decode_input(5, step, 1, sc)))
+        parity.check_y(a, y_or, f"no-alloc call {step} against the oracle")
     ref.close()
 
 
