@@ -664,7 +664,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["pop", "reference"], default="pop")
     ap.add_argument("--workload", default="llama2-7b-ffn-b1", choices=sorted(WORKLOADS))
-    ap.add_argument("--no-secondary", action="store_true", help="skip the B=16 line inside the JSON")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the B=16, 70B-shape and MoE lines inside the default workload's JSON")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="override the workload's decode steps per session (short runs for profiler captures)")
@@ -720,15 +721,23 @@ def main():
     __graft_entry__.build()
 
     res = run_gpu(args.workload, args.steps, args.warmup)
-    secondary = None
+
+    def side_line(name, sessions):
+        s = run_gpu(name, sessions, max(3, args.warmup), with_e2e=False, with_clocks=True)
+        return {"workload": name, "value": s["value"], "unit": UNIT, "sessions": sessions,
+                "decode_only_tokens_per_s": s["decode_only_tokens_per_s"],
+                "decode_step_us": s["decode_step_us"], "kernel_us": s["kernel_us"],
+                "gateup_hbm_gbs": s["gateup_gbs"], "gateup_frac": s["gateup_gbs"] / s["peak"],
+                "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"],
+                "touched_bytes_per_step": s["experts"] * (s["gu_bytes"] + s["dn_bytes"]),
+                "dense_step_us": s["dense_step_us"], "prefill_ms_per_layer": s["prefill_ms_per_layer"],
+                "clocks": s["clocks"]}
+
+    secondary, others = None, []
     if not args.no_secondary and args.workload == "llama2-7b-ffn-b1":
-        s = run_gpu("llama2-7b-ffn-b16", max(3, args.steps // 4), args.warmup, with_e2e=False, with_clocks=False)
-        secondary = {"workload": "llama2-7b-ffn-b16", "value": s["value"], "unit": UNIT,
-                     "decode_only_tokens_per_s": s["decode_only_tokens_per_s"],
-                     "decode_step_us": s["decode_step_us"], "kernel_us": s["kernel_us"],
-                     "gateup_hbm_gbs": s["gateup_gbs"], "gateup_frac": s["gateup_gbs"] / s["peak"],
-                     "step_hbm_gbs": s["step_gbs"], "step_frac": s["step_gbs"] / s["peak"],
-                     "dense_step_us": s["dense_step_us"]}
+        # the batched 7B workload, and the 70B-shape and MoE workloads, each timed over 3 sessions
+        secondary = side_line("llama2-7b-ffn-b16", max(3, args.steps // 4))
+        others = [side_line(n, 3) for n in ("llama-70b-ffn-b64-p16", "moe-8x4096x14336-b32")]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
@@ -763,6 +772,8 @@ def main():
     }
     if secondary:
         line["secondary"] = secondary
+    if others:
+        line["other_workloads"] = others
     print(json.dumps(line), flush=True)
 
 

@@ -35,9 +35,41 @@ def test_every_declared_symbol_is_exported(pop):
     assert set(names) == set(pop.SIGNATURES), "binding and header disagree"
 
 
-def test_library_is_sm103a_build(pop):
-    # the build step compiles for exactly one target; the shared object must exist in-tree
-    assert os.path.exists(pop.LIB_PATH)
+def test_build_targets_sm103a_only(pop, monkeypatch):
+    """Every nvcc command of the build (compile and link) names exactly one target, sm_103a, and
+    the library lands in-tree. The commands are intercepted, not run."""
+    import importlib.util
+    import subprocess
+    spec = importlib.util.spec_from_file_location("_pop_build_t", os.path.join(ROOT, "online_structured_ffn_gb300",
+                                                                              "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    cmds = []
+
+    class Done:
+        returncode, stdout, stderr = 0, "", ""
+
+    def fake_run(cmd, **kw):
+        cmds.append(list(cmd))
+        out = cmd[cmd.index("-o") + 1]
+        open(out, "wb").close()  # stands in for the object or library nvcc would write
+        return Done()
+
+    monkeypatch.setattr(subprocess, "run", fake_run)
+    monkeypatch.setattr(b, "LIB", os.path.join(ROOT, "_pytest_fake_lib.so"))
+    monkeypatch.setattr(b, "BUILD_DIR", os.path.join(ROOT, "_pytest_fake_build"))
+    try:
+        b.build(force=True)
+    finally:
+        import shutil
+        shutil.rmtree(os.path.join(ROOT, "_pytest_fake_build"), ignore_errors=True)
+        if os.path.exists(os.path.join(ROOT, "_pytest_fake_lib.so")):
+            os.remove(os.path.join(ROOT, "_pytest_fake_lib.so"))
+    assert len(cmds) == len(b.sources()) + 1  # one compile per .cu file, one link
+    for c in cmds:
+        targets = [c[i + 1] for i, a in enumerate(c) if a in ("-gencode", "-arch", "--gpu-architecture")]
+        targets += [a for a in c if a.startswith(("-arch=", "--gpu-architecture=", "-gencode="))]
+        assert targets == ["arch=compute_103a,code=sm_103a"], c
     assert os.path.dirname(pop.LIB_PATH).endswith("online_structured_ffn_gb300")
 
 
