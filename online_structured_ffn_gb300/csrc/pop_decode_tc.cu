@@ -8,9 +8,12 @@
 //            y[b][d] = sum over the kept items j (R, then the selected S) of z[b][j] * W2[d, channel of j].
 //
 // The MMA inputs are bf16. x and the weights are bf16 already; z is not, and rounding it to bf16
-// would cost about 3 significant digits of y. So the down GEMM takes z as two bf16 planes, hi =
+// would cost about 3 significant digits of y. So the down GEMM takes z as two bf16 parts, hi =
 // bf16(z) and lo = bf16(z - hi), stacked as 2 x 16..64 token columns of one MMA; the epilogue adds
-// the two halves, which leaves z's own fp32 rounding well below the output tolerance.
+// the two halves, which leaves z's own fp32 rounding well below the output tolerance. The gate/up
+// writes each position's z as one row of 2 NP bf16 (the hi parts of the tokens, then the lo parts),
+// 16-byte stores of one contiguous row per thread; the down GEMM reads those rows as its MN-major
+// B operand, for R (consecutive positions) and for the selected candidates alike.
 //
 // Both are skinny GEMMs with the tokens as the MMA's N (16..64, zero-padded to a multiple of 16)
 // and 128 rows as M. The partition is fixed for a whole decode session, so each partition gets two
@@ -39,13 +42,12 @@
 //
 // Down (k_down_tc): each unit (at most 128 outputs) is split along K over a cluster of `split`
 // CTAs; every CTA streams its share of the R items first (bulk copies from the down slab in the
-// decode, gathered columns in the dense reference path), then gathers its share of the selected
-// items.
+// decode, gathered columns in the dense reference path; their z rows gathered), then gathers its
+// share of the selected items.
 // The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
 // writes the selected positions and channels, and releases a flag. The other CTAs wait (bounded)
-// for the flag when they reach their first selected item. A selected item's z comes as the MMA's
-// MN-major B operand: the gate/up writes each candidate's z as one row of 2 NP bf16 (hi parts of
-// the tokens, then lo parts), which the producers gather like the down columns. The partial accumulators
+// for the flag when they reach their first selected item. Every item's z comes as the MMA's
+// MN-major B operand: the producers gather the z rows like the down columns. The partial accumulators
 // of a split unit are added through distributed shared memory in rank order (a fixed order:
 // results do not depend on timing). No workspace, no atomics on data.
 //
@@ -85,15 +87,12 @@ constexpr int DN_PRE = 2;  // stages of down columns issued before waiting for t
 constexpr int GU_PRE = 2;         // stages of weights issued before waiting for the previous kernel
 
 // Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major). B = z of the
-// 64 items for 2 NP columns (the hi and lo parts of NP tokens): for R items K-major (the z planes,
-// one 128-byte row per column), for selected items MN-major (one 128-byte row per item holding up
-// to 64 columns, atoms of 64 columns 8 KB apart), gathered from the gate/up's candidate rows.
+// 64 items for 2 NP columns (the hi and lo parts of NP tokens), MN-major: one 128-byte row per item
+// holding up to 64 columns, atoms of 64 columns 8 KB apart, gathered from the gate/up's z rows.
 template <int NP>
 struct DnCfg {
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
-  static constexpr uint32_t B_KMAJOR = 2 * NP * TC_BK * 2;
-  static constexpr uint32_t B_MNMAJOR = TC_BK * 128 * ((2 * NP + 63) / 64);
-  static constexpr uint32_t B_BYTES = B_KMAJOR > B_MNMAJOR ? B_KMAJOR : B_MNMAJOR;
+  static constexpr uint32_t B_BYTES = TC_BK * 128 * ((2 * NP + 63) / 64);
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = TC_RING / STAGE_BYTES < 12 ? TC_RING / STAGE_BYTES : 12;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
@@ -118,7 +117,10 @@ constexpr size_t dn_smem_bytes() {
   return 1024 + DnCfg<NP>::STAGES * DnCfg<NP>::STAGE_BYTES;
 }
 
-__device__ __forceinline__ float silu_t(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division: the epilogue of a decode tile runs exposed after its
+// last MMA, and the accurate forms' dependent chains made it several microseconds longer at NP = 64
+// (relative error ~1e-6, far inside the outputs' tolerance and the selection's flagged band).
+__device__ __forceinline__ float silu_t(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ int guard_ch(int v, int n, unsigned* err) {
   if (static_cast<unsigned>(v) >= static_cast<unsigned>(n)) {
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 9..12)
-    pdl_wait();  // z, scores and the z planes may still be read by the previous step's kernels
+    pdl_wait();  // z rows and scores may still be read by the previous step's kernels
     const int q = warp & 3;  // TMEM lane quarter of this warp
     const int half = lane >> 4;
     const int j = 16 * q + (lane & 15);  // position within the unit; lanes 0-15 gate, 16-31 up
@@ -575,21 +577,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int i = 0; i < NH; ++i)
         if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      if (cand) {
+      if (valid) {
+        // the position's z row for the down GEMM: hi parts of the NP tokens, then lo parts
         uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
         store_hilo<NH>(row + b0, row + NP + b0, zz);
-        if (half == 0) a.scores[p] = m * n2v;
-      } else if (valid) {
-#pragma unroll
-        for (int i = 0; i < NH; ++i) {
-          if (b0 + i < a.B) {
-            uint16_t h16, l16;
-            split_bf16(zz[i], h16, l16);
-            const size_t o = static_cast<size_t>(b0 + i) * a.ldk + (p - a.nC);
-            a.zk[o] = h16;
-            a.zk_lo[o] = l16;
-          }
-        }
+        if (cand && half == 0) a.scores[p] = m * n2v;
       }
     }
   }
@@ -868,7 +860,7 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    pdl_wait();  // z, scores and the z planes may still be read by the previous step's kernels
+    pdl_wait();  // z rows and scores may still be read by the previous step's kernels
     const int q = warp & 3;
     const int et = threadIdx.x - 64;  // 0..127
     constexpr int NH = NP / 2;
@@ -922,22 +914,12 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
         for (int i = 0; i < NH; ++i)
           if (b0 + i < a.B) m = fmaxf(m, fabsf(zz[i]));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (cand) {
-          // the candidate's row of the selected items' operand: hi parts of tokens [0, NP), then lo
+        if (valid) {
+          // the position's z row for the down GEMM (its MN-major operand): hi parts of tokens
+          // [0, NP), then lo parts
           uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
           store_hilo<NH>(row + b0, row + NP + b0, zz);
-          if (half == 0) a.scores[p] = m * n2v;
-        } else if (valid) {
-#pragma unroll
-          for (int i = 0; i < NH; ++i) {
-            if (b0 + i < a.B) {
-              uint16_t h16, l16;
-              split_bf16(zz[i], h16, l16);
-              const size_t o = static_cast<size_t>(b0 + i) * a.ldk + (p - a.nC);
-              a.zk[o] = h16;
-              a.zk_lo[o] = l16;
-            }
-          }
+          if (cand && half == 0) a.scores[p] = m * n2v;
         }
       } else {
         float gv[NP], uv[NP];
@@ -964,22 +946,9 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
             zz[b] = silu_t(gv[b]) * uv[b];
             if (b < a.B) m = fmaxf(m, fabsf(zz[b]));
           }
-          if (cand) {
-            uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
-            store_hilo<NP>(row, row + NP, zz);
-            a.scores[p] = m * n2v;
-          } else {
-#pragma unroll
-            for (int b = 0; b < NP; ++b) {
-              if (b < a.B) {
-                uint16_t h16, l16;
-                split_bf16(zz[b], h16, l16);
-                const size_t o = static_cast<size_t>(b) * a.ldk + (p - a.nC);
-                a.zk[o] = h16;
-                a.zk_lo[o] = l16;
-              }
-            }
-          }
+          uint16_t* row = a.zcp + static_cast<size_t>(p) * (2 * NP);
+          store_hilo<NP>(row, row + NP, zz);
+          if (cand) a.scores[p] = m * n2v;
         }
       }
     }
@@ -1057,7 +1026,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   if (a.sel && ci == 0) {
     // ------------------------------------------------------------ the selecting cluster
     if (rank == 0) {
-      pdl_wait();  // this step's scores and z; S, memory, step and the z planes of the previous step
+      pdl_wait();  // this step's scores and z rows; S, memory and step of the previous step
       pdl_trigger();
       down_select(a, smem, rsc);
     }
@@ -1105,7 +1074,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   const uint32_t tmem_base = ctl.tmem_base;
   pdl_trigger();
   // Only the producers touch this step's data before the epilogue (which follows their copies
-  // through the barriers); they wait for the previous kernel before the z planes (see below).
+  // through the barriers); they wait for the previous kernel before the z rows (see below).
 
   auto fail = [&]() {
     if (!*abort_flag) {
@@ -1122,12 +1091,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     // of R or of S are zero-filled, as are token rows past B. Each warp keeps the channels of its
     // items for DN_WIN stages in shared memory, fetched together (one round of loads per window).
     // The down columns and the channels of R are constant between partitions, so the A copies of
-    // the first stages go out before griddepcontrol.wait; their z planes follow it.
+    // the first stages go out before griddepcontrol.wait; their z rows follow it.
     const int cq = lane & 7, grp = (warp * 32 + lane) >> 3;
     const int pt = warp * 32 + lane;
     const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(a.D);
     const size_t row3 = 3 * static_cast<size_t>(a.D);
-    const uint16_t* zk_lo = a.zk + a.zk_lo_off;
     const int h = grp & 1, ip = (grp & 3) >> 1;  // output half; item parity within the warp's pair
     const int nrs = r1 - r0;                     // R stages of each unit
     int* mywin = dwin + warp * (DN_WIN * 8);
@@ -1203,19 +1171,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         issue_bs(bi, sa);
         return;
       }
-      const int kb = r0 + bi;  // column block of the z planes
-      // chunk c = pt + 256 v -> plane c / (8 NP), token row (c / 8) % NP, chunk c % 8
+      // R stage: the z rows of R items 64 kb .. 64 kb + 63 (list positions r_pos0 + item, contiguous),
+      // in the same MN-major layout as the selected items'; items past the end of R read as zero
+      constexpr int CPI = NP / 4;
+      const int kb = r0 + bi;
 #pragma unroll
-      for (int v = 0; v < NP / 16; ++v) {
-        const int c = pt + TC_PROD_THREADS * v;
-        const int plane = c / (8 * NP), b = (c >> 3) % NP, zq = c & 7;
-        const uint32_t nb = b < a.B ? 16u : 0u;
-        const uint16_t* zsrc = (plane ? zk_lo : a.zk) + static_cast<size_t>(b) * a.ldk + kb * TC_BK + 8 * zq;
-        cp_async16(sa + Cfg::A_BYTES + plane * (NP * 128) + b * 128 + ((zq ^ (b & 7)) << 4), nb ? zsrc : a.zk, nb);
+      for (int v = 0; v < CPI / 4; ++v) {
+        const int qd = lane + 32 * v;
+        const int e = qd / CPI, c = qd % CPI;
+        const int i = 2 * warp + (e & 1) + 16 * (e >> 1);
+        const int item = kb * TC_BK + i;
+        const uint32_t nb = item < a.nR ? 16u : 0u;
+        cp_async16(sa + Cfg::A_BYTES + (c >> 3) * (TC_BK * 128) + i * 128 + (((c & 7) ^ (i & 7)) << 4),
+                   nb ? a.zcp + static_cast<size_t>(a.r_pos0 + item) * (2 * NP) + 8 * c : a.zcp, nb);
       }
     };
     // stages whose A copies go out before the wait: the first DN_PRE R stages of the first unit (more
-    // only queue behind the memory system's back-pressure and hold the z planes, and so the MMAs, back)
+    // only queue behind the memory system's back-pressure and hold the z rows, and so the MMAs, back)
     const int pre = unit0 < U ? min(DN_PRE, min(STAGES, nrs)) : 0;
     if (pre == 0) pdl_wait();
     uint32_t issued = 0;
@@ -1294,7 +1266,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         }
         if (issued < static_cast<uint32_t>(pre)) {
           if (issued + 1 == static_cast<uint32_t>(pre)) {
-            // the z planes of this step exist once the previous kernel has finished
+            // the z rows of this step exist once the previous kernel has finished
             pdl_wait();
             for (int bj = 0; bj < pre; ++bj) {
               issue_b(slab ? (bj + 7 * unit) % nrs : bj, smem_u32(smem + bj * STAGE_BYTES));
@@ -1308,7 +1280,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         ++issued;
       }
     }
-    // an abort before the wait still owes the z planes of the first stages nothing: their barriers
+    // an abort before the wait still owes the z rows of the first stages nothing: their barriers
     // are only drained below through the copies of this warp
     if (issued < static_cast<uint32_t>(pre)) pdl_wait();
     if (!a.sel && a.count_step && blockIdx.x == 0 && threadIdx.x == 0) *a.step += 1;
@@ -1326,8 +1298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
   } else if (warp == TC_MMA_WARP) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
-      const uint32_t idesc = idesc_bf16_f32(TC_BM, 2 * NP, false, true);
-      const uint32_t idesc_s = idesc_bf16_f32(TC_BM, 2 * NP, true, true);  // selected: B MN-major too
+      const uint32_t idesc_s = idesc_bf16_f32(TC_BM, 2 * NP, true, true);  // A and B MN-major
       const int nrs = r1 - r0;
       uint32_t consumed = 0;
       int it = 0;
@@ -1352,22 +1323,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
           fence_proxy_async();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-          // descriptors once per stage: a K step of 16 items moves A by 2048 bytes (+128), and B by 32
-          // bytes (+2) when K-major (R) or, like A, 2048 bytes when MN-major (selected items)
+          // descriptors once per stage: a K step of 16 items moves A and B (both MN-major) by 2048
+          // bytes (+128)
           const uint64_t ad = smem_desc_sw128(sa, TC_BK * 128, 1024u);
-          if (bi < nrs) {
-            const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, 16u, 1024u);
-            umma_f16(d_tmem, ad, bd, idesc, bi > 0 ? 1u : 0u);
-            umma_f16(d_tmem, ad + 128, bd + 2, idesc, 1u);
-            umma_f16(d_tmem, ad + 256, bd + 4, idesc, 1u);
-            umma_f16(d_tmem, ad + 384, bd + 6, idesc, 1u);
-          } else {
-            const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, TC_BK * 128, 1024u);
-            umma_f16(d_tmem, ad, bd, idesc_s, bi > 0 ? 1u : 0u);
-            umma_f16(d_tmem, ad + 128, bd + 128, idesc_s, 1u);
-            umma_f16(d_tmem, ad + 256, bd + 256, idesc_s, 1u);
-            umma_f16(d_tmem, ad + 384, bd + 384, idesc_s, 1u);
-          }
+          const uint64_t bd = smem_desc_sw128(sa + Cfg::A_BYTES, TC_BK * 128, 1024u);
+          umma_f16(d_tmem, ad, bd, idesc_s, bi > 0 ? 1u : 0u);
+          umma_f16(d_tmem, ad + 128, bd + 128, idesc_s, 1u);
+          umma_f16(d_tmem, ad + 256, bd + 256, idesc_s, 1u);
+          umma_f16(d_tmem, ad + 384, bd + 384, idesc_s, 1u);
           umma_commit(&ctl.empty[s]);
           ++consumed;
         }

@@ -43,10 +43,8 @@ struct pop_ffn {
   float* ypart = nullptr;  // B = 1 down: partial tiles [chunks][D]
   int ypart_parts = 0;     // capacity in units of D floats
   // B > 1 decode (tensor-core kernels)
-  uint16_t* zk = nullptr;  // [2][max_batch][ldk]: bf16 hi and lo parts of z of the kept items (R, then S)
-  int ldk = 0;
   int* ch_s = nullptr;     // channels of the selected candidates, in S order
-  uint16_t* zcp = nullptr; // [N][2 * round_up(max_batch, 16)]: the candidates' z rows (hi, lo), B > 1
+  uint16_t* zcp = nullptr; // [N][2 * round_up(max_batch, 16)]: every list position's z row (hi, lo), B > 1
   int* rcs = nullptr;      // skip variant: [C[S] | R], the list of the steps between updates
   long long host_step = 0; // decode steps since the last partition (the device step counter's mirror)
   // B > 1 decode slabs (rebuilt at every partition): gate/up rows of R u C and down columns of R
@@ -132,7 +130,7 @@ void prof_end(pop_ffn* h) {
 
 void free_all(pop_ffn* h) {
   void* ptrs[] = {h->Wp,    h->n2,   h->Z,     h->part,    h->sumsq, h->I,      h->rc,     h->P,
-                  h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->zk,     h->ch_s,
+                  h->idx_all, h->z, h->scores, h->memory, h->S,     h->ypart,  h->ch_s,
                   h->step, h->err,     h->fsync, h->gu_slab, h->dn_slab, h->zcp, h->rcs, h->gu_slab_skip};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -206,9 +204,6 @@ pop_status gateup_slab(pop_ffn* h, const uint16_t* x, int B, cudaStream_t st, bo
   a.nR = h->cnt.n_R;
   a.n2 = h->n2;
   a.zcp = h->zcp;
-  a.zk = h->zk;
-  a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
-  a.ldk = h->ldk;
   a.scores = h->scores;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
@@ -231,9 +226,6 @@ pop_status gateup_tc(pop_ffn* h, const uint16_t* x, int B, const int* rc, int nC
   a.nR = nR;
   a.n2 = h->n2;
   a.zcp = h->zcp;
-  a.zk = h->zk;
-  a.zk_lo = h->zk + static_cast<size_t>(h->cfg.max_batch) * h->ldk;
-  a.ldk = h->ldk;
   a.scores = h->scores;
   a.err = h->err;
   a.wait_ns = h->wait_ns;
@@ -264,9 +256,9 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   a.k = k;
   a.ch_r = ch_r;
   a.ch_s = h->ch_s;
-  a.zk = h->zk;
-  a.zk_lo_off = static_cast<size_t>(h->cfg.max_batch) * h->ldk;
-  a.ldk = h->ldk;
+  // R's z rows follow the list's candidates: |C| of the partition, the held selection's k on a skip
+  // step, none in the dense path (every channel is an R item there)
+  a.r_pos0 = decode ? (skip ? k : h->cnt.n_C) : 0;
   a.y = y;
   a.out_f32 = h->cfg.out_f32;
   a.dslab = decode ? h->dn_slab : nullptr;
@@ -397,7 +389,6 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   h->ldZ = round_up(N, 128);
   h->ldPart = h->ldZ;
   h->ypart_parts = 2 * h->num_sms;
-  h->ldk = round_up(N + 128, 8);  // the selected items start at a 64-aligned column after R
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   auto bail = [&](cudaError_t err, const char* where) {
@@ -426,7 +417,6 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
   POP_ALLOC(h->rcs, N);
   POP_ALLOC(h->ypart, static_cast<size_t>(h->ypart_parts) * D);
   if (cfg->max_batch > 1) {
-    POP_ALLOC(h->zk, 2 * static_cast<size_t>(cfg->max_batch) * h->ldk);
     POP_ALLOC(h->ch_s, N);
     POP_ALLOC(h->zcp, static_cast<size_t>(N) * 2 * round_up(cfg->max_batch, 16));
     h->gu_geom = gu_slab_geom(cnt.n_C + cnt.n_R, D, h->num_sms);
@@ -445,10 +435,6 @@ pop_status pop_ffn_create(const pop_config* cfg, const void* Wg, const void* W1,
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->err, 0, sizeof(unsigned), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   if (h->ch_s && (e = cudaMemsetAsync(h->ch_s, 0, sizeof(int) * N, st)) != cudaSuccess)
-    return bail(e, "cudaMemsetAsync");
-  // the z planes' columns between R and the selected items are read (against zero weights): keep
-  // them finite
-  if (h->zk && (e = cudaMemsetAsync(h->zk, 0, 2 * sizeof(uint16_t) * cfg->max_batch * h->ldk, st)) != cudaSuccess)
     return bail(e, "cudaMemsetAsync");
   if ((e = cudaMemsetAsync(h->step, 0, sizeof(int), st)) != cudaSuccess) return bail(e, "cudaMemsetAsync");
   // index lists always hold valid positions, even before the first partition or selection

@@ -37,11 +37,8 @@ struct GateUpTcArgs {
   const int* rc;         // position -> channel: [C | R]
   int nC, nR;
   const float* n2;       // ||W2[:, c]||
-  uint16_t* zcp;         // out: z of the candidate positions as rows of 2 NP bf16 (hi parts of the
-                         // tokens, then lo parts), [nC][2 NP]
-  uint16_t* zk;          // out: z of R as bf16 hi parts at [b][p - nC] (row stride ldk)
-  uint16_t* zk_lo;       // ... and bf16 lo parts z - hi
-  int ldk;
+  uint16_t* zcp;         // out: z of every position p as row p of 2 NP bf16 (hi parts of the tokens,
+                         // then lo parts z - hi), [nC + nR][2 NP]
   float* scores;         // out: [nC]
   // work split (set by the launcher)
   int units, rows_cap, ks, stages;
@@ -57,16 +54,14 @@ struct DownTcArgs {
   int k;                 // selected candidates
   const int* ch_r;       // channels of R (ascending)
   int* ch_s;             // channels of the selected candidates (written by the selecting CTA)
-  const uint16_t* zk;    // z planes: hi [b][ldk], lo at zk + zk_lo_off
-  size_t zk_lo_off;
-  int ldk;
+  int r_pos0;            // list position of R item 0: its z row is zcp row r_pos0 + item
   void* y;               // out: [B][D], fp32 or bf16
   int out_f32;
   const uint16_t* dslab; // down slab of R (units are then the 128-output slices of the slab), or NULL
   // selection by the first cluster (sel = 1, decode with candidates)
   int sel;
   const float* scores;   // [nC] this step's candidate scores
-  const uint16_t* zcp;   // [nC][2 NP] candidates' z rows (hi, lo) from the gate/up
+  const uint16_t* zcp;   // [positions][2 NP] z rows (hi, lo) from the gate/up
   const int* rc;         // position -> channel, C first
   int nC, period;
   float* memory;
@@ -130,11 +125,8 @@ struct GateUpSlabArgs {
   const int* rc;         // for the candidates' down-column norms
   int nC, nR;
   const float* n2;
-  uint16_t* zcp;         // out: the candidates' z rows, [nC][2 NP] bf16 (hi parts of the NP tokens,
-                         // then their lo parts), the down GEMM's MN-major operand for selected items
-  uint16_t* zk;
-  uint16_t* zk_lo;
-  int ldk;
+  uint16_t* zcp;         // out: every position's z row, [nC + nR][2 NP] bf16 (hi parts of the NP
+                         // tokens, then their lo parts), the down GEMM's MN-major operand
   float* scores;
   int ks, stages;        // set by the launcher
   unsigned* err;
