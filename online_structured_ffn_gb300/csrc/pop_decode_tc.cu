@@ -962,46 +962,41 @@ __global__ void __launch_bounds__(GS_THREADS, 1)
   }
 }
 
-// One epilogue thread's part of a split unit's reduction: the NP / SK tokens [b0, b0 + NP / SK) of
-// one output row d, from the partial rows of all SK CTAs of the cluster (16-byte distributed
-// shared-memory reads, all issued before the first add), added in rank order and stored to y.
+// The epilogue threads' part of a split unit's reduction. The partials sit token-major in each
+// CTA's shared memory (pb[t * 128 + row]), so four consecutive rows of one token are one 16-byte
+// word. CTA `rank` finishes rows [rank * 128 / SK, (rank + 1) * 128 / SK) of the unit; an item is
+// (token t, group of 4 rows): its SK partial words are read from every CTA of the cluster (all loads
+// before the first add), added in rank order and stored to y as 4 consecutive outputs. Consecutive
+// threads take consecutive row groups of one token, so a warp stores whole runs of y.
 template <int NP, int SK>
-__device__ __forceinline__ void cluster_finish_row(const DownTcArgs& a, uint32_t pbase, int b0, int d, bool dok) {
-  constexpr int TPT = NP / SK;
-  static_assert(TPT % 2 == 0, "tokens per thread");
-  constexpr int W = TPT % 4 == 0 ? 4 : 2;  // floats per load
-  constexpr int L = TPT / W;               // loads per peer
-  float v[SK][TPT];
+__device__ __forceinline__ void cluster_finish(const DownTcArgs& a, uint32_t pb, uint32_t rank, int et, int d_lo,
+                                               int d_hi) {
+  constexpr int ROWS = TC_BM / SK, RG = ROWS / 4, ITEMS = RG * NP;
+  static_assert(ROWS % 4 == 0, "row groups of 4");
+#pragma unroll 1
+  for (int it = et; it < ITEMS; it += 128) {
+    const int t = it / RG, rg = it % RG;
+    const int row = static_cast<int>(rank) * ROWS + 4 * rg;
+    const uint32_t off = pb + static_cast<uint32_t>(t * TC_BM + row) * 4u;
+    float4 v[SK];
 #pragma unroll
-  for (int pr = 0; pr < SK; ++pr) {
-    const uint32_t base = map_peer(pbase, static_cast<uint32_t>(pr)) + 4u * b0;
+    for (int pr = 0; pr < SK; ++pr) v[pr] = ld_peer4(map_peer(off, static_cast<uint32_t>(pr)));
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int l = 0; l < L; ++l) {
-      if (W == 4) {
-        const float4 t = ld_peer4(base + 16u * l);
-        v[pr][4 * l] = t.x;
-        v[pr][4 * l + 1] = t.y;
-        v[pr][4 * l + 2] = t.z;
-        v[pr][4 * l + 3] = t.w;
-      } else {
-        const float2 t = ld_peer2(base + 8u * l);
-        v[pr][2 * l] = t.x;
-        v[pr][2 * l + 1] = t.y;
-      }
+    for (int pr = 0; pr < SK; ++pr) {
+      g.x += v[pr].x;
+      g.y += v[pr].y;
+      g.z += v[pr].z;
+      g.w += v[pr].w;
     }
-  }
-  if (!dok) return;
-#pragma unroll
-  for (int j = 0; j < TPT; ++j) {
-    float g = 0.f;
-#pragma unroll
-    for (int pr = 0; pr < SK; ++pr) g += v[pr][j];
-    const int bb = b0 + j;
-    if (bb < a.B) {
-      if (a.out_f32)
-        static_cast<float*>(a.y)[static_cast<size_t>(bb) * a.D + d] = g;
-      else
-        static_cast<__nv_bfloat16*>(a.y)[static_cast<size_t>(bb) * a.D + d] = __float2bfloat16_rn(g);
+    const int d = d_lo + row;  // units hold whole groups of 8 outputs: d < d_hi implies d + 3 < d_hi
+    if (t < a.B && d < d_hi) {
+      const size_t o = static_cast<size_t>(t) * a.D + d;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.y) + o) = g;
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.y) + o) = make_uint2(pack_bf16x2(g.x, g.y), pack_bf16x2(g.z, g.w));
+      }
     }
   }
 }
@@ -1375,10 +1370,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
       if (lane == 0) mbar_arrive(&ctl.tempty[buf]);
       if (SK > 1) {
         // partial of a split unit: to this CTA's shared memory (the stage ring, idle by now: all
-        // copies landed and all MMAs finished), rows of NP floats
-        float* pb = reinterpret_cast<float*>(smem) + r * NP;
+        // copies landed and all MMAs finished), token-major: pb[t * 128 + row]
+        float* pb = reinterpret_cast<float*>(smem) + r;
 #pragma unroll
-        for (int c = 0; c < NP; ++c) pb[c] = yv[c];
+        for (int c = 0; c < NP; ++c) pb[c * TC_BM] = yv[c];
         continue;
       }
       const int d = unit_lo(unit) + r;
@@ -1398,23 +1393,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
 
   if (SK > 1) {
     // ------------------------------------------------------------ cluster reduction of the split unit
-    // Every thread of the cluster passes both barriers. Between them, epilogue thread et of rank
-    // `rank` finishes row rank * 128 / SK + et / SK for tokens [part * NP / SK, (part + 1) * NP / SK),
-    // part = et % SK, adding the SK partials in rank order.
+    // Every thread of the cluster passes both barriers. Between them the epilogue threads of rank
+    // `rank` finish its share of the unit's rows (cluster_finish), adding the SK partials in rank order.
     cluster_sync_all();
     if (warp >= TC_EPI0 && unit0 < U && !*abort_flag) {
       const int et = threadIdx.x - 32 * TC_EPI0;
-      const int rows_per = TC_BM / SK, tpt = NP / SK;
-      const int rl = et / SK, part = et % SK;
-      const int row = static_cast<int>(rank) * rows_per + rl;
-      const int b0 = part * tpt;
-      const int d = unit_lo(unit0) + row;
-      const bool dok = d < unit_lo(unit0 + 1);
-      const uint32_t pbase = smem_u32(smem) + static_cast<uint32_t>(row * NP) * 4u;
+      const uint32_t pb = smem_u32(smem);
+      const int d_lo = unit_lo(unit0), d_hi = unit_lo(unit0 + 1);
       switch (SK) {
-        case 2: cluster_finish_row<NP, 2>(a, pbase, b0, d, dok); break;
-        case 4: cluster_finish_row<NP, 4>(a, pbase, b0, d, dok); break;
-        default: cluster_finish_row<NP, 8>(a, pbase, b0, d, dok); break;
+        case 2: cluster_finish<NP, 2>(a, pb, rank, et, d_lo, d_hi); break;
+        case 4: cluster_finish<NP, 4>(a, pb, rank, et, d_lo, d_hi); break;
+        default: cluster_finish<NP, 8>(a, pb, rank, et, d_lo, d_hi); break;
       }
     }
     cluster_sync_all();  // no CTA leaves while a peer may still read its partials
