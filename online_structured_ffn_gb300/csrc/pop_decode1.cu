@@ -19,12 +19,20 @@
 // launch, and the result does not depend on timing.
 //
 // Both kernels are launched with programmatic dependent launch when the caller's stream allows it.
-// Before waiting for the previous kernel (griddepcontrol.wait) they touch constant data only: L2
-// prefetches of weight rows, and in the down kernel the channel ids of R, which only a partition
-// changes; a partition is written by ordinary launches that have completed before the gate/up
-// grid passes its wait, and the gate/up grid lets the down grid start only after that wait. x, z
-// and S are read and z, S, y written only after the wait, so the overlap with the previous
-// kernel's tail never races on data.
+// Before waiting for the previous kernel (griddepcontrol.wait) they touch constant data only: in
+// the gate/up kernel an L2 prefetch of each warp's first load group, in the down kernel the
+// channel ids of R, which only a partition changes; a partition is written by ordinary launches
+// that have completed before the gate/up grid passes its wait, and the gate/up grid lets the down
+// grid start only after that wait. x, z and S are read and z, S, y written only after the wait,
+// so the overlap with the previous kernel's tail never races on data.
+//
+// The prefetch is kept small on purpose. CTAs that become resident during the previous kernel's
+// tail share the memory system with it: a whole 16 KB channel per warp (80 MB over the grid) held
+// back the previous grid's completion, and with it this grid's wait, by about 3 us, and an L2
+// prefetch of all of R's down slices in the down kernel slowed the gate/up tail it overlapped by
+// more than it saved. B = 1 decode step at the LLaMA-2-7B FFN shape: 42.2 us with both, 38.5 us
+// with 2 KB + 2 KB per warp and no down prefetch, 37.4 us with the down slices of 32 retained
+// items per CTA added (1 + 1 KB per gate/up warp: 39.2 us; 4 + 4 KB: 39.0 us; 64 items: 37.6 us).
 #include "pop_device.cuh"
 #include "pop_internal.h"
 #include "pop_radix.cuh"
@@ -39,6 +47,7 @@ constexpr int DT_TILE = 512;   // outputs per tile: 64 threads x 8
 constexpr int DT_GROUPS = DT_THREADS / (DT_TILE / 8);
 constexpr int DT_BATCH = 512;  // kept channels staged in shared memory at a time
 constexpr int DT_UNROLL = 8;
+constexpr int DT_PREFETCH = 32;  // retained items per down CTA whose slices are prefetched before the wait
 
 struct BlockSync256 {
   __device__ void operator()() const { __syncthreads(); }
@@ -160,15 +169,18 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
   const int r0 = rb0 + warp * (rb1 - rb0) / GS_WARPS, r1 = rb0 + (warp + 1) * (rb1 - rb0) / GS_WARPS;
   const int nch = D >> 3;
   const size_t row3 = 3 * static_cast<size_t>(D);
-  // constant data only before the wait: warm L2 with this warp's first channel (on a skip step
-  // the list's head, the held selection, may be written by the kernel before: R only)
+  constexpr int GRP = NCHL < 4 ? NCHL : 4;  // 16-byte loads per lane and row in flight at once
+  // constant data only before the wait: warm L2 with the first load group of this warp's first
+  // channel, GRP x 512 bytes of its gate row and of its up row, one 128-byte line per lane (on a
+  // skip step the list's head, the held selection, may be written by the kernel before: R only)
   {
     const int p = c0 < c1 && !a.skip ? c0 : (r0 < r1 ? r0 : -1);
-    if (p >= 0) {
+    if (p >= 0 && lane < 4 * GRP && 64 * lane < D) {
       const int ch = __ldcg(a.rc + p);
       if (static_cast<unsigned>(ch) < static_cast<unsigned>(a.N)) {
-        const uint8_t* row = reinterpret_cast<const uint8_t*>(a.Wp + static_cast<size_t>(ch) * row3);
-        for (int off = lane * 128; off < 4 * D; off += 32 * 128) prefetch_l2(row + off);
+        const uint16_t* rg = a.Wp + static_cast<size_t>(ch) * row3 + 64 * lane;
+        prefetch_l2(rg);
+        prefetch_l2(rg + D);
       }
     }
   }
@@ -180,7 +192,6 @@ __global__ void __launch_bounds__(GS_THREADS, 4) k_gateup_sel_b1(const __grid_co
     reinterpret_cast<float4*>(xs + 8 * c)[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
   }
   __syncthreads();
-  constexpr int GRP = NCHL < 4 ? NCHL : 4;
 
   auto item = [&](int p) {
     const int ch = guard_idx(__ldcg(a.rc + p), a.N, a.err);
@@ -254,8 +265,8 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   const int grp = threadIdx.x / (DT_TILE / 8), tt = threadIdx.x % (DT_TILE / 8);
   const int d = tile * DT_TILE + 8 * tt;
   const bool dok = d < D;
-  // chunk c takes the c-th share of R and the c-th share of S, so every CTA has the same mix of
-  // prefetched (R) and not prefetched (S) columns
+  // chunk c takes the c-th share of R and the c-th share of S, so every CTA streams the same
+  // number of columns
   const unsigned uc = static_cast<unsigned>(chunk), un = static_cast<unsigned>(NCK);
   const int r_lo = static_cast<int>(uc * static_cast<unsigned>(a.nR) / un);
   const int nr = static_cast<int>((uc + 1u) * static_cast<unsigned>(a.nR) / un) - r_lo;
@@ -269,17 +280,17 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   // Constant data only before the wait: the channel ids of the first batch's retained items (R
   // never changes between partitions, and a partition is written by an ordinary launch that has
-  // finished before this grid's primary started), and an L2 prefetch of their down slices, one
-  // 128-byte line per thread and round.
+  // finished before this grid's primary started), and an L2 prefetch of the down slices of the
+  // first DT_PREFETCH of them, one 128-byte line per thread.
   const int nr0 = min(DT_BATCH, nr);
   for (int e = threadIdx.x; e < nr0; e += DT_THREADS) s_ch[e] = guard_idx(__ldcg(a.rc + a.nC + r_lo + e), a.N, a.err);
   __syncthreads();
   {
     constexpr int LPS = DT_TILE * 2 / 128;  // 128-byte lines per tile slice
-    for (int q = threadIdx.x; q < nr0 * LPS; q += DT_THREADS) {
-      const int dd = tile * DT_TILE + (q % LPS) * 64;
-      if (dd < D) prefetch_l2(W2 + static_cast<size_t>(s_ch[q / LPS]) * row3 + dd);
-    }
+    static_assert(DT_PREFETCH * LPS <= DT_THREADS, "one prefetch per thread");
+    const int q = threadIdx.x;
+    const int dd = tile * DT_TILE + (q % LPS) * 64;
+    if (q < min(nr0, DT_PREFETCH) * LPS && dd < D) prefetch_l2(W2 + static_cast<size_t>(s_ch[q / LPS]) * row3 + dd);
   }
   pdl_trigger();
   pdl_wait();
