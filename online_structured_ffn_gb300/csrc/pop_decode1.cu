@@ -358,14 +358,27 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   const int e4 = tile * DT_TILE + 4 * qc;
   float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (e4 < D) {
-    // D is a multiple of 8, so a float4 column inside y lies wholly inside it
-#pragma unroll 8
-    for (int c = sub; c < NCK; c += NSUB) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ypart + static_cast<size_t>(c) * D + e4));
-      t4.x += v.x;
-      t4.y += v.y;
-      t4.z += v.z;
-      t4.w += v.w;
+    // D is a multiple of 8, so a float4 column inside y lies wholly inside it. The chunks are
+    // loaded 12 at a time (a 7B-sized tile has 38 chunks: one round of loads per thread) and
+    // added in chunk order.
+    constexpr int RL = 12;
+    for (int c0 = sub; c0 < NCK; c0 += RL * NSUB) {
+      float4 v[RL];
+#pragma unroll
+      for (int u = 0; u < RL; ++u) {
+        const int c = c0 + u * NSUB;
+        v[u] = c < NCK ? __ldcg(reinterpret_cast<const float4*>(a.ypart + static_cast<size_t>(c) * D + e4))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < RL; ++u) {
+        if (c0 + u * NSUB < NCK) {
+          t4.x += v[u].x;
+          t4.y += v[u].y;
+          t4.z += v[u].z;
+          t4.w += v[u].w;
+        }
+      }
     }
   }
   reinterpret_cast<float4*>(&red[sub][0])[qc] = t4;

@@ -83,7 +83,10 @@ constexpr int GU_MAX_ROWS = 64;  // positions per unit (gate + up = 128 MMA rows
 // down: per producer warp, the channels of its 8 items of each of DN_WIN k-blocks
 constexpr int DN_WIN = 32;
 constexpr int DN_WIN_WORDS = 8 * DN_WIN * 8;
-constexpr int DN_PRE = 2;  // stages of down columns issued before waiting for the previous kernel
+// stages of down columns issued before waiting for the previous kernel: none. Issued early, they
+// held the CTAs' wait back by about 2 us, longer than they saved (LLaMA-2-7B FFN shape, B = 16:
+// step 40.2 us with 2, 39.2 us with 1, 38.6 us with none).
+constexpr int DN_PRE = 0;
 constexpr int GU_PRE = 2;         // stages of weights issued before waiting for the previous kernel
 
 // Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major). B = z of the
