@@ -214,11 +214,6 @@ __device__ __forceinline__ float4 ld_peer4(uint32_t addr) {
                : "memory");
   return v;
 }
-__device__ __forceinline__ float2 ld_peer2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
 
 // barrier over the eight producer warps (the selecting CTA uses the same warps)
 struct ProdSync {
@@ -1091,7 +1086,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     // The down columns and the channels of R are constant between partitions, so the A copies of
     // the first stages go out before griddepcontrol.wait; their z rows follow it.
     const int cq = lane & 7, grp = (warp * 32 + lane) >> 3;
-    const int pt = warp * 32 + lane;
     const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(a.D);
     const size_t row3 = 3 * static_cast<size_t>(a.D);
     const int h = grp & 1, ip = (grp & 3) >> 1;  // output half; item parity within the warp's pair
@@ -1297,7 +1291,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
       const uint32_t idesc_s = idesc_bf16_f32(TC_BM, 2 * NP, true, true);  // A and B MN-major
-      const int nrs = r1 - r0;
       uint32_t consumed = 0;
       int it = 0;
       bool ok = true;
