@@ -41,9 +41,12 @@
 // previous kernel.
 //
 // Down (k_down_tc): each unit (at most 128 outputs) is split along K over a cluster of `split`
-// CTAs; every CTA streams its share of the R items first (bulk copies from the down slab in the
-// decode, gathered columns in the dense reference path; their z rows gathered), then gathers its
-// share of the selected items.
+// CTAs; every CTA streams its share of the R items first, then gathers its share of the selected
+// items. In the decode one thread brings an R stage: a bulk copy of its slab tile and TMA boxes of
+// its z rows (contiguous rows of the list); the eight producer warps gather the selected stages
+// (and, in the dense reference path, every stage). A stage that all eight warps had to issue, each
+// with its own barrier and copy instructions, took about 0.5 us of issue time whatever its size,
+// which capped the R stream at about 40 KB per microsecond per CTA.
 // The first cluster does the selection meanwhile: its CTA 0 updates the memory, takes the top-k,
 // writes the selected positions and channels, and releases a flag. The other CTAs wait (bounded)
 // for the flag when they reach their first selected item. Every item's z comes as the MMA's
@@ -83,10 +86,6 @@ constexpr int GU_MAX_ROWS = 64;  // positions per unit (gate + up = 128 MMA rows
 // down: per producer warp, the channels of its 8 items of each of DN_WIN k-blocks
 constexpr int DN_WIN = 32;
 constexpr int DN_WIN_WORDS = 8 * DN_WIN * 8;
-// stages of down columns issued before waiting for the previous kernel: none. Issued early, they
-// held the CTAs' wait back by about 2 us, longer than they saved (LLaMA-2-7B FFN shape, B = 16:
-// step 40.2 us with 2, 39.2 us with 1, 38.6 us with none).
-constexpr int DN_PRE = 0;
 constexpr int GU_PRE = 2;         // stages of weights issued before waiting for the previous kernel
 
 // Down stage: one k-block; A = 64 items x 128 outputs (two 64-wide halves, MN-major). B = z of the
@@ -95,7 +94,8 @@ constexpr int GU_PRE = 2;         // stages of weights issued before waiting for
 template <int NP>
 struct DnCfg {
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
-  static constexpr uint32_t B_BYTES = TC_BK * 128 * ((2 * NP + 63) / 64);
+  static constexpr int ZATOMS = (2 * NP + 63) / 64;  // 64-column atoms of the z rows
+  static constexpr uint32_t B_BYTES = TC_BK * 128 * ZATOMS;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = TC_RING / STAGE_BYTES < 12 ? TC_RING / STAGE_BYTES : 12;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
@@ -1001,7 +1001,8 @@ __device__ __forceinline__ void cluster_finish(const DownTcArgs& a, uint32_t pb,
 
 // ------------------------------------------------------------------ selection + down over R u S
 template <int NP>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant__ DownTcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_down_tc(const __grid_constant__ CUtensorMap mapZ, const __grid_constant__ DownTcArgs a) {
   using Cfg = DnCfg<NP>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr uint32_t STAGE_BYTES = Cfg::STAGE_BYTES;
@@ -1061,6 +1062,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     tmem_alloc(&ctl.tmem_base, TC_TMEM_COLS);
     tmem_relinquish();
   }
+  if (threadIdx.x == 0 && slab) prefetch_tmap(&mapZ);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1083,8 +1085,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     // items' 256 contiguous bytes; the z-plane chunks (NP / 16 per lane) follow. Items past the end
     // of R or of S are zero-filled, as are token rows past B. Each warp keeps the channels of its
     // items for DN_WIN stages in shared memory, fetched together (one round of loads per window).
-    // The down columns and the channels of R are constant between partitions, so the A copies of
-    // the first stages go out before griddepcontrol.wait; their z rows follow it.
     const int cq = lane & 7, grp = (warp * 32 + lane) >> 3;
     const uint16_t* W2 = a.Wp + 2 * static_cast<size_t>(a.D);
     const size_t row3 = 3 * static_cast<size_t>(a.D);
@@ -1178,10 +1178,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
                    nb ? a.zcp + static_cast<size_t>(a.r_pos0 + item) * (2 * NP) + 8 * c : a.zcp, nb);
       }
     };
-    // stages whose A copies go out before the wait: the first DN_PRE R stages of the first unit (more
-    // only queue behind the memory system's back-pressure and hold the z rows, and so the MMAs, back)
-    const int pre = unit0 < U ? min(DN_PRE, min(STAGES, nrs)) : 0;
-    if (pre == 0) pdl_wait();
+    // Nothing goes out before the wait for the previous kernel: slab copies issued early held the
+    // CTAs' wait back by about 2 us, longer than they saved (LLaMA-2-7B FFN shape, B = 16: step
+    // 40.2 us with two stages issued early, 38.6 us with none).
+    pdl_wait();
     uint32_t issued = 0;
     bool ok = true;
     for (int unit = unit0; unit < U && ok; unit += nunits) {
@@ -1232,9 +1232,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         // R blocks from the slab go in an order rotated per unit (the units of a rank read the same z
         // columns; in step they would ask L2 for the same lines at once)
         const int rb = from_slab ? (bi + 7 * unit) % nrs : bi;
-        if (!from_slab && (bi < wlo || bi >= whi)) fill(bi);
         const int s = issued % STAGES;
         const uint32_t ph = (issued / STAGES) & 1u;
+        if (from_slab) {
+          // R stage: warp 0 lane 0 alone; its barrier counts the slab tile and the z boxes (rows of
+          // items past the end of R lie outside the map and read as zero)
+          if (warp == 0) {
+            int good = 1;
+            if (lane == 0) {
+              if (!mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, a.wait_ns, abort_flag)) {
+                fail();
+                good = 0;
+              } else {
+                uint8_t* st = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&ctl.afull[s], Cfg::A_BYTES + Cfg::B_BYTES);
+                bulk_g2s(st, a.dslab + (static_cast<size_t>(unit) * a.kbr + r0 + rb) * (Cfg::A_BYTES / 2),
+                         Cfg::A_BYTES, &ctl.afull[s]);
+                for (int at = 0; at < Cfg::ZATOMS; ++at)
+                  tma_load_2d(st + Cfg::A_BYTES + at * (TC_BK * 128), &mapZ, &ctl.afull[s], 64 * at,
+                              a.r_pos0 + (r0 + rb) * TC_BK);
+              }
+            }
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+              ok = false;
+              break;
+            }
+          }
+          ++issued;
+          continue;
+        }
+        if (bi < wlo || bi >= whi) fill(bi);
         bool got = true;
         if (lane == 0) {
           got = mbar_wait_bounded(&ctl.empty[s], ph ^ 1u, a.wait_ns, abort_flag);
@@ -1245,36 +1272,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
           ok = false;
           break;
         }
+        // gathered stage (the selected items; every stage of the dense path): all eight warps, one
+        // arrival per thread once its copies have landed
         const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        if (from_slab) {
-          if (warp == 0 && lane == 0) {
-            mbar_arrive_expect_tx(&ctl.afull[s], Cfg::A_BYTES);
-            bulk_g2s(smem + s * STAGE_BYTES, a.dslab + (static_cast<size_t>(unit) * a.kbr + r0 + rb) * (Cfg::A_BYTES / 2),
-                     Cfg::A_BYTES, &ctl.afull[s]);
-          }
-        } else {
-          if (warp == 0 && lane == 0) mbar_arrive(&ctl.afull[s]);
-          issue_a(bi, sa, d0, dok);
-        }
-        if (issued < static_cast<uint32_t>(pre)) {
-          if (issued + 1 == static_cast<uint32_t>(pre)) {
-            // the z rows of this step exist once the previous kernel has finished
-            pdl_wait();
-            for (int bj = 0; bj < pre; ++bj) {
-              issue_b(slab ? (bj + 7 * unit) % nrs : bj, smem_u32(smem + bj * STAGE_BYTES));
-              cp_async_arrive(&ctl.full[bj]);
-            }
-          }
-        } else {
-          issue_b(rb, sa);
-          cp_async_arrive(&ctl.full[s]);
-        }
+        if (warp == 0 && lane == 0) mbar_arrive(&ctl.afull[s]);
+        issue_a(bi, sa, d0, dok);
+        issue_b(rb, sa);
+        cp_async_arrive(&ctl.full[s]);
         ++issued;
       }
     }
-    // an abort before the wait still owes the z rows of the first stages nothing: their barriers
-    // are only drained below through the copies of this warp
-    if (issued < static_cast<uint32_t>(pre)) pdl_wait();
     if (!a.sel && a.count_step && blockIdx.x == 0 && threadIdx.x == 0) *a.step += 1;
     // every copy this warp started must land before the CTA can exit (the slab tiles: through their
     // barriers, for the last STAGES stages issued; earlier ones were consumed by the MMAs)
@@ -1291,7 +1298,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer (one thread)
       const uint32_t idesc_s = idesc_bf16_f32(TC_BM, 2 * NP, true, true);  // A and B MN-major
+      const int nrs = r1 - r0;
       uint32_t consumed = 0;
+      uint32_t fph = 0;  // per slot: parity of the next phase of full[], which only gathered stages use
       int it = 0;
       bool ok = true;
       for (int unit = unit0; unit < U && ok; unit += nunits, ++it) {
@@ -1305,12 +1314,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_down_tc(const __grid_constant
         for (int bi = 0; bi < nblk; ++bi) {
           const int s = consumed % STAGES;
           const uint32_t ph = (consumed / STAGES) & 1u;
-          if (!mbar_wait_bounded(&ctl.full[s], ph, a.wait_ns, abort_flag) ||
+          const bool gathered = !(slab && bi < nrs);
+          if ((gathered && !mbar_wait_bounded(&ctl.full[s], (fph >> s) & 1u, a.wait_ns, abort_flag)) ||
               !mbar_wait_bounded(&ctl.afull[s], ph, a.wait_ns, abort_flag)) {
             fail();
             ok = false;
             break;
           }
+          if (gathered) fph ^= 1u << s;
           fence_proxy_async();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
@@ -1482,7 +1493,7 @@ cudaError_t launch_gateup_np(const CUtensorMap& xm, GateUpTcArgs a, int num_sms,
 // rows x k-blocks, with units of at least 64 outputs where possible (shorter runs per gathered
 // column cost DRAM efficiency); ties go to the smaller split.
 template <int NP>
-cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
+cudaError_t launch_down_np(const CUtensorMap& zm, DownTcArgs a, int num_sms, cudaStream_t st) {
   // the ring, or the selecting CTA's keys (|C| of them) if those need more
   size_t smem = dn_smem_bytes<NP>();
   constexpr size_t kStatic = sizeof(TcCtl) + sizeof(RadixScratch<TC_PROD_THREADS>) + 2 * sizeof(int) * DN_WIN_WORDS + 64;
@@ -1522,7 +1533,7 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
     a.units = 0;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(1);
-    return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, a);
+    return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, zm, a);
   }
   // The split depends only on these sizes and the device: computed once per shape (the occupancy
   // queries cost host time on every step otherwise).
@@ -1604,7 +1615,7 @@ cudaError_t launch_down_np(DownTcArgs a, int num_sms, cudaStream_t st) {
     const int ctas = best_u < num_sms - sel ? best_u : num_sms - sel;
     cfg.gridDim = dim3((ctas > 0 ? ctas : 1) + sel);
   }
-  return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, a);
+  return cudaLaunchKernelEx(&cfg, k_down_tc<NP>, zm, a);
 }
 }  // namespace
 
@@ -1760,12 +1771,12 @@ cudaError_t launch_gateup_tc(const CUtensorMap& x_map, GateUpTcArgs args, int nu
   }
 }
 
-cudaError_t launch_down_tc(DownTcArgs args, int num_sms, cudaStream_t st) {
+cudaError_t launch_down_tc(const CUtensorMap& z_map, DownTcArgs args, int num_sms, cudaStream_t st) {
   switch (args.NP) {
-    case 16: return launch_down_np<16>(args, num_sms, st);
-    case 32: return launch_down_np<32>(args, num_sms, st);
-    case 48: return launch_down_np<48>(args, num_sms, st);
-    case 64: return launch_down_np<64>(args, num_sms, st);
+    case 16: return launch_down_np<16>(z_map, args, num_sms, st);
+    case 32: return launch_down_np<32>(z_map, args, num_sms, st);
+    case 48: return launch_down_np<48>(z_map, args, num_sms, st);
+    case 64: return launch_down_np<64>(z_map, args, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

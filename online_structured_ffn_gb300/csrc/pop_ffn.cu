@@ -283,7 +283,10 @@ pop_status down_tc(pop_ffn* h, int B, const int* ch_r, int nR, int k, bool decod
   }
   a.err = h->err;
   a.wait_ns = h->wait_ns;
-  POP_CUDA(h, launch_down_tc(a, h->num_sms, st));
+  CUtensorMap zm;
+  if (!encode_zrows_map(&zm, h->zcp, a.r_pos0 + nR, a.NP))
+    return fail(h, POP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed for the z rows");
+  POP_CUDA(h, launch_down_tc(zm, a, h->num_sms, st));
   return POP_OK;
 }
 

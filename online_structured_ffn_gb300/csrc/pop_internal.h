@@ -30,6 +30,9 @@ cudaError_t launch_pack(const uint16_t* Wg, const uint16_t* W1, const uint16_t* 
 // The B operand of a decode GEMM: `rows` token rows of `inner` bf16, `ld` elements apart, box
 // {64, NP} (rows NP > `rows` read as zero).
 bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int NP);
+// The z rows of the list as the down GEMM's B operand: `rows` rows of 2 NP bf16 (hi then lo parts),
+// box {64, 64} (columns past 2 NP and rows past `rows` read as zero).
+bool encode_zrows_map(CUtensorMap* m, const uint16_t* zcp, int rows, int NP);
 struct GateUpTcArgs {
   const uint16_t* Wp;    // packed weights
   int D, N;
@@ -134,7 +137,9 @@ struct GateUpSlabArgs {
 };
 cudaError_t launch_gateup_slab(const CUtensorMap& x_map, GateUpSlabArgs args, int num_sms, cudaStream_t st);
 // the selection (when args.sel), then y = sum over R and the selected items of z W2[:, channel]
-cudaError_t launch_down_tc(DownTcArgs args, int num_sms, cudaStream_t st);
+// z_map: the z rows as a bf16 [r_pos0 + nR][2 NP] tensor, box {64, 64}, 128-byte swizzle
+// (encode_zrows_map); the decode's R stages load their z rows through it.
+cudaError_t launch_down_tc(const CUtensorMap& z_map, DownTcArgs args, int num_sms, cudaStream_t st);
 
 // ---- decode step for B = 1 (pop_decode1.cu): gate/up with in-kernel top-k, tiled down
 struct DecodeB1Args {

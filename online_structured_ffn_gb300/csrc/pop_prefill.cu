@@ -361,6 +361,11 @@ bool encode_z_map(CUtensorMap* m, const uint16_t* Z, int M, int N, int ldZ) {
   return encode_2d(m, Z, N, M, static_cast<uint64_t>(ldZ) * 2, BK, BM);
 }
 
+bool encode_zrows_map(CUtensorMap* m, const uint16_t* zcp, int rows, int NP) {
+  return encode_2d(m, zcp, static_cast<uint64_t>(2 * NP), static_cast<uint64_t>(rows > 0 ? rows : 1),
+                   static_cast<uint64_t>(4 * NP), 64, 64);
+}
+
 bool encode_tokens_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int NP) {
   return encode_2d(m, base, static_cast<uint64_t>(inner), static_cast<uint64_t>(rows), static_cast<uint64_t>(ld) * 2,
                    64, static_cast<uint32_t>(NP));
