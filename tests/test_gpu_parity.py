@@ -160,6 +160,20 @@ def test_decode_parity_shapes(env, D, N):
     lay.close()
 
 
+@pytest.mark.parametrize("N", [105, 106, 108, 211, 213, 215])
+def test_decode_r_block_edges(env, N):
+    # |R| = 63, 64, 65, 127, 128, 129 at r = 0.3, gamma = 0.1: the last 64-item block of R is short
+    # by one item, exactly full, or holds one item, so the z rows past R (which the B > 1 down GEMM
+    # loads as zero) are checked at every edge; B = 16 and 64 cover one and two 64-column z atoms.
+    lay = Layer(env, 264, N, r=0.3, gamma=0.1, max_batch=64)
+    assert lay.counts.n_R == {105: 63, 106: 64, 108: 65, 211: 127, 213: 128, 215: 129}[N]
+    Wg, W1, W2 = lay.w64()
+    ref = oracle.prefill(Wg, W1, W2, f64(synth.prompt(0, 16, lay.sc)), 0.3, 0.1)
+    for B in (16, 64):
+        _decode_session(env, lay, (ref["R"], ref["C"], ref["P"]), B, steps=2)
+    lay.close()
+
+
 @pytest.mark.parametrize("D,N,r,gamma,period", [(512, 2048, 0.3, 0.1, 1), (4096, 11008, 0.299, 0.1, 1),
                                                 (256, 1024, 0.5, 0.1, 4), (1024, 600, 0.3, 0.0, 1),
                                                 (1024, 600, 0.4, 0.6, 1), (2048, 333, 0.0, 0.1, 1),
