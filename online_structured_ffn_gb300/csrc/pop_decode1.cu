@@ -12,11 +12,12 @@
 // costs no time on the critical path. Progress is guaranteed: the workers wait on nobody, so CTA 0
 // never holds up a CTA it waits for, even when the grid does not fit on the GPU at once.
 //
-// Launch 2, k_down_tiled_b1: y = sum over R u S of z_i W2[:, i]. CTA (t, c) owns the 512-wide
-// tile t of y and the c-th chunk of the kept channels; 8 groups of 64 threads each read one
-// channel's 1 KB slice of the contiguous down column with 16-byte loads. The last chunk CTA to
+// Launch 2, k_down_tiled_b1: y = sum over R u S of z_i W2[:, i]. CTA (t, c) owns the 256-wide
+// tile t of y and the c-th chunk of the kept channels; 16 groups of 32 threads each read one
+// channel's 512-byte slice of the contiguous down column with 16-byte loads. The last chunk CTA to
 // finish a tile (atomic counter) adds the chunks' partial tiles in a fixed order: no extra
-// launch, and the result does not depend on timing.
+// launch, and the result does not depend on timing. (512-wide tiles, twice the chunks per tile,
+// were 0.2 us slower per step at the LLaMA-2-7B FFN shape; 1024-wide ones 4.3 us.)
 //
 // Both kernels are launched with programmatic dependent launch when the caller's stream allows it.
 // Before waiting for the previous kernel (griddepcontrol.wait) they touch constant data only: in
@@ -31,8 +32,8 @@
 // back the previous grid's completion, and with it this grid's wait, by about 3 us, and an L2
 // prefetch of all of R's down slices in the down kernel slowed the gate/up tail it overlapped by
 // more than it saved. B = 1 decode step at the LLaMA-2-7B FFN shape: 42.2 us with both, 38.5 us
-// with 2 KB + 2 KB per warp and no down prefetch, 37.4 us with the down slices of 32 retained
-// items per CTA added (1 + 1 KB per gate/up warp: 39.2 us; 4 + 4 KB: 39.0 us; 64 items: 37.6 us).
+// with 2 KB + 2 KB per warp and no down prefetch, 37.4 us with 32 KB of down slices per down CTA
+// added (1 + 1 KB per gate/up warp: 39.2 us; 4 + 4 KB: 39.0 us; 64 KB: 37.6 us).
 #include "pop_device.cuh"
 #include "pop_internal.h"
 #include "pop_radix.cuh"
@@ -43,11 +44,11 @@ namespace {
 constexpr int GS_THREADS = 256;
 constexpr int GS_WARPS = GS_THREADS / 32;
 constexpr int DT_THREADS = 512;
-constexpr int DT_TILE = 512;   // outputs per tile: 64 threads x 8
+constexpr int DT_TILE = 256;   // outputs per tile: 32 threads x 8
 constexpr int DT_GROUPS = DT_THREADS / (DT_TILE / 8);
 constexpr int DT_BATCH = 512;  // kept channels staged in shared memory at a time
 constexpr int DT_UNROLL = 8;
-constexpr int DT_PREFETCH = 32;  // retained items per down CTA whose slices are prefetched before the wait
+constexpr int DT_PREFETCH = 64;  // retained items per down CTA whose slices are prefetched before the wait
 
 struct BlockSync256 {
   __device__ void operator()() const { __syncthreads(); }
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(DT_THREADS, 2) k_down_tiled_b1(const __grid_co
   float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (e4 < D) {
     // D is a multiple of 8, so a float4 column inside y lies wholly inside it. The chunks are
-    // loaded 12 at a time (a 7B-sized tile has 38 chunks: one round of loads per thread) and
+    // loaded 12 at a time (a 7B-sized tile has 19 chunks: one round of loads per thread) and
     // added in chunk order.
     constexpr int RL = 12;
     for (int c0 = sub; c0 < NCK; c0 += RL * NSUB) {
