@@ -388,6 +388,10 @@ class MoeStack:
     def check(self):
         self.moe.check()
 
+    def set_profiling(self, on):
+        # the experts run one after another while their kernels are timed one by one
+        self.moe.set_concurrent(not on)
+
     def close(self):
         self.moe.close()
 
@@ -428,6 +432,8 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     for f in stack.ffn:
         f.check()
     # profiled pass: the same sessions with events between the kernels of every decode step
+    if hasattr(stack, "set_profiling"):
+        stack.set_profiling(True)
     for f in stack.ffn:
         f.profile(1)
     for _ in range(PROFILE_SESSIONS):
@@ -437,6 +443,8 @@ def run_gpu(wl_name, steps, warmup, with_e2e=True, with_clocks=True):
     for f in stack.ffn:
         f.profile(False)
         f.check()
+    if hasattr(stack, "set_profiling"):
+        stack.set_profiling(False)
     B, T, Lyr = wl["B"], wl["T"], wl["layers"]
     dense_us = dense_step_us(stack) if not wl.get("experts") else None
     units = B * T * Lyr * steps

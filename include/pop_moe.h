@@ -58,10 +58,20 @@ pop_status pop_moe_prefill_partition(pop_moe_t m, const void* X, const float* lo
  * y device [B, D] (dtype per out_f32), 1 <= B <= max_batch. Every expert runs pop_decode_step on
  * a [B, D] input holding its routed tokens in ascending token order followed by zero rows (a zero
  * row has z = 0, so it changes neither the batch-max scores nor the routed tokens' outputs).
- * No allocation and no host synchronization: 2 + 2 * n_experts kernels on `stream` (the skip
- * variant's update steps add, per expert at B > 1, the rebuild of its slab's selected tiles).
+ * No allocation and no host synchronization: 2 + 2 * n_experts kernels (the skip variant's
+ * update steps add, per expert at B > 1, the rebuild of its slab's selected tiles). The routing
+ * and the combine run on `stream`; the experts' kernels run as pop_moe_set_concurrent sets, and
+ * the call is stream-ordered on `stream` either way (CUDA-graph capture included).
  * STATE if no partition has been set. */
 pop_status pop_moe_decode_step(pop_moe_t m, const void* x, const float* logits, int B, void* y, void* stream);
+
+/* How the experts' decode kernels are scheduled. on != 0 (the default): each expert runs on a
+ * stream of its own that the handle owns, forked from the caller's stream after the routing (an
+ * event) and joined back before the combine, so that one expert's kernels overlap another's;
+ * the experts share no data, so y does not change. on = 0: the experts run one after another on
+ * the caller's stream, so that per-kernel timing (pop_profile_enable on the experts) times each
+ * kernel alone. INVALID_ARG for a NULL handle. */
+pop_status pop_moe_set_concurrent(pop_moe_t m, int on);
 
 /* Routing of the last prefill or decode call: host int experts[T][2] and float weights[T][2]
  * (either may be NULL); *T receives the number of tokens of that call. Syncs. STATE before the

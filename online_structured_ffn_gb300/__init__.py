@@ -77,6 +77,7 @@ SIGNATURES = {
     "pop_moe_expert": (_vp, [_vp, _i32]),
     "pop_moe_num_experts": (_i32, [_vp]),
     "pop_moe_check": (_i32, [_vp]),
+    "pop_moe_set_concurrent": (_i32, [_vp, _i32]),
     "pop_moe_last_error": (ctypes.c_char_p, [_vp]),
 }
 
@@ -451,6 +452,11 @@ class PopMoE:
 
     def check(self):
         _check_moe(load_library().pop_moe_check(self.handle), self.handle)
+
+    def set_concurrent(self, on: bool):
+        """Experts' decode kernels on streams of their own (True, the default) or one after another
+        on the caller's stream (False: for per-kernel timing)."""
+        _check_moe(load_library().pop_moe_set_concurrent(self.handle, 1 if on else 0), self.handle)
 
 
 load_library()

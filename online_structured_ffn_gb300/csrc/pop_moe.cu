@@ -29,6 +29,12 @@ struct pop_moe {
   int* offsets = nullptr;  // [E + 1] first grouped row of each expert (prefill)
   float* zeros = nullptr;  // [N] importance of an expert without prompt tokens
   unsigned* err = nullptr; // device error word of the routing kernels
+  // decode: each expert's two kernels run on a stream of their own, forked from the caller's stream
+  // after the routing and joined before the combine (the experts share no data)
+  std::vector<cudaStream_t> xs;
+  std::vector<cudaEvent_t> xev;  // [E] each expert's step done
+  cudaEvent_t fork = nullptr;    // the routing of this step done
+  bool concurrent = true;        // pop_moe_set_concurrent
   int last_T = 0;
   bool partitioned = false;
   std::string msg;
@@ -304,6 +310,12 @@ void free_moe(pop_moe* m) {
   for (pop_ffn_t h : m->ex)
     if (h) pop_ffn_destroy(h);
   m->ex.clear();
+  for (cudaStream_t q : m->xs) cudaStreamDestroy(q);
+  m->xs.clear();
+  for (cudaEvent_t v : m->xev) cudaEventDestroy(v);
+  m->xev.clear();
+  if (m->fork) cudaEventDestroy(m->fork);
+  m->fork = nullptr;
   cudaFree(m->xe);
   cudaFree(m->ye);
   cudaFree(m->r_ex);
@@ -376,6 +388,15 @@ pop_status pop_moe_create(const pop_config* cfg, int n_experts, const void* cons
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, sizeof(unsigned));
   if (e == cudaSuccess) e = cudaMemset(m->counts, 0, sizeof(int) * n_experts);
   if (e == cudaSuccess) e = alloc_routes(m, cfg->max_batch);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->fork, cudaEventDisableTiming);
+  for (int x = 0; x < n_experts && e == cudaSuccess; ++x) {
+    cudaStream_t q = nullptr;
+    cudaEvent_t v = nullptr;
+    e = cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking);
+    if (e == cudaSuccess) m->xs.push_back(q);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    if (e == cudaSuccess) m->xev.push_back(v);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_moe(m);
@@ -476,16 +497,31 @@ pop_status pop_moe_decode_step(pop_moe_t m, const void* x, const float* logits, 
   MOE_CUDA(m, launch_moe_pdl(k_moe_route_scatter, dim3(B, E), dim3(MOE_THREADS), st, static_cast<const uint16_t*>(x),
                              logits, B, E, D, m->xe, m->r_ex, m->r_w, m->r_slot, m->counts));
   const size_t per = static_cast<size_t>(B) * D;
+  if (m->concurrent) MOE_CUDA(m, cudaEventRecord(m->fork, st));
   for (int e = 0; e < E; ++e) {
-    const pop_status s = pop_decode_step(m->ex[e], m->xe + e * per, B, m->ye + e * per, st);
+    cudaStream_t es = st;
+    if (m->concurrent) {
+      es = m->xs[e];
+      MOE_CUDA(m, cudaStreamWaitEvent(es, m->fork, 0));
+    }
+    const pop_status s = pop_decode_step(m->ex[e], m->xe + e * per, B, m->ye + e * per, es);
     if (s != POP_OK) return moe_expert_fail(m, s, e);
+    if (m->concurrent) MOE_CUDA(m, cudaEventRecord(m->xev[e], es));
   }
+  if (m->concurrent)
+    for (int e = 0; e < E; ++e) MOE_CUDA(m, cudaStreamWaitEvent(st, m->xev[e], 0));
   dim3 grid(B, (D / 4 + MOE_THREADS - 1) / MOE_THREADS);
   MOE_CUDA(m, launch_moe_pdl(k_moe_combine, grid, dim3(MOE_THREADS), st, static_cast<const int*>(m->r_ex),
                              static_cast<const float*>(m->r_w), static_cast<const int*>(m->r_slot),
                              static_cast<const int*>(nullptr), B, E, E * B, static_cast<const float*>(m->ye), D, y,
                              m->cfg.out_f32, m->err));
   m->last_T = B;
+  return POP_OK;
+}
+
+pop_status pop_moe_set_concurrent(pop_moe_t m, int on) {
+  if (!m) return moe_fail(nullptr, POP_ERR_INVALID_ARG, "pop_moe_set_concurrent: NULL handle");
+  m->concurrent = on != 0;
   return POP_OK;
 }
 

@@ -137,6 +137,30 @@ def test_moe_prefill_and_decode(env, B):
     m.close()
 
 
+def test_moe_concurrent_equals_serial(env):
+    # the experts' decode kernels on streams of their own (the default) or one after another on the
+    # caller's stream: the same bits, step after step (periodic memory, so the steps carry state)
+    _, torch, dev = env
+    E, D, N, B, steps = 4, 256, 1024, 16, 6
+    m = Moe(env, E, D, N, r=0.3, gamma=0.1, period=4, max_batch=B, max_prefill_tokens=32)
+    X = synth.prompt(m.seed, 64, m.sc)
+    L = synth.router_logits(m.seed, 64, E).astype(np.float32)
+    m.moe.prefill_partition(up(env, X), logits_t(env, L), torch.empty((64, D), dtype=torch.float32, device=dev))
+    parts = [m.moe.experts[e].partition() for e in range(E)]
+    ys = {}
+    for concurrent in (True, False):
+        m.moe.set_concurrent(concurrent)
+        for e in range(E):
+            m.moe.experts[e].set_partition(*parts[e])
+        ys[concurrent] = [m.moe.decode_step(up(env, synth.decode_input(m.seed, t, B, m.sc)),
+                                            logits_t(env, synth.router_logits(m.seed, B, E, step=t))).cpu().numpy()
+                          for t in range(steps)]
+    m.moe.check()
+    for t in range(steps):
+        assert np.array_equal(ys[True][t].view(np.uint32), ys[False][t].view(np.uint32)), f"step {t}"
+    m.close()
+
+
 def test_moe_idle_experts(env):
     """Experts that get no prompt token split by the index tie rule; in decode they select the
     lowest candidate positions and contribute nothing."""
