@@ -165,6 +165,7 @@ def test_moe_rejects_bad_arguments_before_touching_cuda(pop):
     assert lib.pop_moe_get_routing(None, ctypes.byref(T), None, None) == pop.POP_ERR_INVALID_ARG
     assert lib.pop_moe_expert(None, 0) is None
     assert lib.pop_moe_num_experts(None) == -1
+    assert lib.pop_moe_set_concurrent(None, 1) == pop.POP_ERR_INVALID_ARG
     lib.pop_moe_destroy(None)  # no-op
 
 
