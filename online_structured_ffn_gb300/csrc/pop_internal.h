@@ -166,7 +166,7 @@ struct DecodeB1Args {
   void* y;
   int out_f32;
   unsigned* sync;      // 1 counter: candidates scored so far (0 between launches)
-  unsigned* tile_cnt;  // per 512-wide tile of y: chunk CTAs done (0 between launches)
+  unsigned* tile_cnt;  // per output tile of y: chunk CTAs done (0 between launches)
   unsigned* err;
   uint64_t wait_ns;
 };
