@@ -267,23 +267,26 @@ class Stack:
             dec_events[1].record()
 
     def session_e2e(self, hX, hx, hY, hy):
-        """The same session with inputs in pinned host memory, outputs copied back, all timed."""
+        """The same session with inputs in pinned host memory and every output copied back, all
+        timed (see overlapped_copies)."""
         pop, torch = self.pop, self.torch
-        st = torch.cuda.current_stream().cuda_stream
+        cs = torch.cuda.current_stream()
+        st = cs.cuda_stream
         B, T = self.wl["B"], self.wl["T"]
-        for l, f in enumerate(self.ffn):
-            self.X[l].copy_(hX[l], non_blocking=True)
-            pop.pop_prefill_partition(f.handle, self.X[l].data_ptr(), self.X[l].shape[0], self.Y[l].data_ptr(), st)
-            hY[l].copy_(self.Y[l], non_blocking=True)
         lib = pop.load_library()
-        for t in range(T):
-            self.x[t].copy_(hx[t], non_blocking=True)
+        with OverlappedCopies(torch, cs) as oc:
+            ready = [oc.up(self.X[l], hX[l]) for l in range(len(self.ffn))]
             for l, f in enumerate(self.ffn):
-                s = lib.pop_decode_step(f.handle, self.x[t, l].data_ptr(), B, self.y[t, l].data_ptr(), st)
-                if s:
-                    pop._check(s, f.handle)
-            hy[t].copy_(self.y[t], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+                cs.wait_event(ready[l])
+                pop.pop_prefill_partition(f.handle, self.X[l].data_ptr(), self.X[l].shape[0], self.Y[l].data_ptr(), st)
+                oc.down(hY[l], self.Y[l])
+            for t in range(T):
+                self.x[t].copy_(hx[t], non_blocking=True)  # each step's input right before the step
+                for l, f in enumerate(self.ffn):
+                    s = lib.pop_decode_step(f.handle, self.x[t, l].data_ptr(), B, self.y[t, l].data_ptr(), st)
+                    if s:
+                        pop._check(s, f.handle)
+                oc.down(hy[t], self.y[t])
 
     def close(self):
         for f in self.ffn:
@@ -362,22 +365,23 @@ class MoeStack:
 
     def session_e2e(self, hX, hx, hY, hy):
         pop, torch = self.pop, self.torch
-        st = torch.cuda.current_stream().cuda_stream
+        cs = torch.cuda.current_stream()
+        st = cs.cuda_stream
         B, T = self.wl["B"], self.wl["T"]
-        self.X[0].copy_(hX[0], non_blocking=True)
-        self.Lp.copy_(self.hLp, non_blocking=True)
-        self.moe.prefill_partition(self.X[0], self.Lp, self.Y[0])
-        hY[0].copy_(self.Y[0], non_blocking=True)
         lib = pop.load_library()
-        for t in range(T):
-            self.x[t].copy_(hx[t], non_blocking=True)
-            self.L[t].copy_(self.hL[t], non_blocking=True)
-            s = lib.pop_moe_decode_step(self.moe.handle, self.x[t].data_ptr(), self.L[t].data_ptr(), B,
-                                        self.y[t].data_ptr(), st)
-            if s:
-                pop._check_moe(s, self.moe.handle)
-            hy[t].copy_(self.y[t], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        with OverlappedCopies(torch, cs) as oc:
+            self.X[0].copy_(hX[0], non_blocking=True)
+            self.Lp.copy_(self.hLp, non_blocking=True)
+            self.moe.prefill_partition(self.X[0], self.Lp, self.Y[0])
+            oc.down(hY[0], self.Y[0])
+            for t in range(T):
+                self.x[t].copy_(hx[t], non_blocking=True)  # each step's input right before the step
+                self.L[t].copy_(self.hL[t], non_blocking=True)
+                s = lib.pop_moe_decode_step(self.moe.handle, self.x[t].data_ptr(), self.L[t].data_ptr(), B,
+                                            self.y[t].data_ptr(), st)
+                if s:
+                    pop._check_moe(s, self.moe.handle)
+                oc.down(hy[t], self.y[t])
 
     def e2e_extra_h2d(self):
         """Pinned host copies of the router logits; returns their bytes per session."""
@@ -394,6 +398,55 @@ class MoeStack:
 
     def close(self):
         self.moe.close()
+
+
+class OverlappedCopies:
+    """Host<->device copies of an end-to-end session on two side streams, ordered against the
+    compute stream by events: inputs known up front (the prompts) go up while earlier work runs,
+    and every result goes down once the compute stream has produced it, while later work runs. A
+    decode step's input stays on the compute stream right before the step, since in a model it
+    depends on the previous step's output. Leaving the block waits for every copy, so the next
+    session's kernels never overwrite a buffer that is still being copied out."""
+
+    _streams = {}
+
+    def __init__(self, torch, compute_stream):
+        self.torch, self.cs = torch, compute_stream
+        dev = compute_stream.device
+        if dev not in OverlappedCopies._streams:
+            OverlappedCopies._streams[dev] = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        self.up_s, self.down_s = OverlappedCopies._streams[dev]
+
+    def __enter__(self):
+        # the side streams start after the work already queued on the compute stream
+        ev = self.torch.cuda.Event()
+        ev.record(self.cs)
+        self.up_s.wait_event(ev)
+        self.down_s.wait_event(ev)
+        return self
+
+    def up(self, dst, src):
+        """Copies src (pinned host) to dst on the upload stream; returns the event that marks it."""
+        with self.torch.cuda.stream(self.up_s):
+            dst.copy_(src, non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record(self.up_s)
+        return ev
+
+    def down(self, dst, src):
+        """Copies src to dst (pinned host) on the download stream once the compute stream's work so
+        far is done."""
+        ev = self.torch.cuda.Event()
+        ev.record(self.cs)
+        self.down_s.wait_event(ev)
+        with self.torch.cuda.stream(self.down_s):
+            dst.copy_(src, non_blocking=True)
+
+    def __exit__(self, *exc):
+        self.cs.synchronize()
+        self.up_s.synchronize()
+        self.down_s.synchronize()
+        return False
 
 
 def make_stack(wl):
