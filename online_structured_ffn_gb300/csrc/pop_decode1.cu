@@ -44,7 +44,8 @@ namespace {
 constexpr int GS_THREADS = 256;
 constexpr int GS_WARPS = GS_THREADS / 32;
 constexpr int DT_THREADS = 512;
-constexpr int DT_TILE = 256;   // outputs per tile: 32 threads x 8
+constexpr int DT_TILE = B1_DOWN_TILE;  // outputs per tile: 32 threads x 8
+static_assert(DT_TILE == 256, "the thread layout below assumes 256-wide tiles");
 constexpr int DT_GROUPS = DT_THREADS / (DT_TILE / 8);
 constexpr int DT_BATCH = 512;  // kept channels staged in shared memory at a time
 constexpr int DT_UNROLL = 8;

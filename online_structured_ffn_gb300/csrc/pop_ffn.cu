@@ -71,8 +71,8 @@ struct pop_ffn {
 
 static constexpr int kProfEvents = 5;
 // device counters: [4] candidates scored by the B = 1 gate/up, [5] the B > 1 selection flag, [8..]
-// tiles of y done by the B = 1 down chunks
-static constexpr int kSyncWords = 64;
+// tiles of y done by the B = 1 down chunks (one per tile, up to the widest D)
+static constexpr int kSyncWords = 8 + pop::b1_down_tiles(POP_MAX_D);
 static constexpr int kProfMaxSteps = 256;
 
 namespace {

@@ -171,6 +171,9 @@ struct DecodeB1Args {
   uint64_t wait_ns;
 };
 int down_tiled_chunks(int D, int nitems, int num_sms);
+// B = 1 down: outputs per tile of y; the handle keeps one inter-CTA counter per tile
+constexpr int B1_DOWN_TILE = 256;
+constexpr int b1_down_tiles(int D) { return (D + B1_DOWN_TILE - 1) / B1_DOWN_TILE; }
 cudaError_t launch_gateup_sel_b1(const DecodeB1Args& a, int grid, cudaStream_t st);
 cudaError_t launch_down_tiled_b1(const DecodeB1Args& a, int num_sms, cudaStream_t st);
 
